@@ -1,0 +1,147 @@
+/*
+ * m3scan.h -- C ABI of libm3scan.so, the B300 (sm_103a) Mamba-3 selective
+ * SSM scan: a chunked prefill (m3_scan_fwd) and a single-token decode step
+ * (m3_step).
+ *
+ * The operation (Mamba-3 summary page, "Mamba-3: Expressive SSM with MIMO"):
+ * for every batch row b and head h independently, with scalar A_h < 0 and
+ *
+ *   alpha_t = exp(dt_t A_h), beta_t = (1 - lambda_t) dt_t alpha_t,
+ *   gamma_t = lambda_t dt_t                       (§3.1.1, eq. (5)-(6))
+ *   u_t     = sum_r B_t[r] x_t[r]^T   (N x P)     (§3.3, MIMO rank R)
+ *   h'_t    = Rot(theta_t) (alpha_t h'_{t-1} + beta_t u_{t-1}) + gamma_t u_t
+ *   y_t[r]  = C_t[r]^T h'_t
+ *
+ * where Rot(theta_t) rotates every state row pair (2k, 2k+1), k < N/2, by the
+ * angle theta_t[k]:  (a, b) -> (a cos - b sin, a sin + b cos)  -- the complex
+ * state of §3.2 (Proposition 3.2.1) written as real 2x2 blocks.  theta_t is the
+ * per-step angle and already includes dt.  The prefill computes it in the
+ * rotated (data-dependent RoPE) frame of Propositions 3.2.2 / 3.2.3, with the
+ * trapezoid mask of eq. (7); the state it returns is in the complex frame
+ * above, the same frame m3_step reads and writes, so decode continues a
+ * prefill directly.  lambda = 1 and theta = 0 give the Mamba-2 (SSD) update.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are CUDA device pointers (device memory or managed memory the
+ *    device can read) owned by the caller, C-contiguous and aligned to their
+ *    element size; the fp32 state / final_state must be 16-byte aligned, and
+ *    the tensor-core prefill (M3_ALGO_CHUNKED_TC) also needs x, B, C, theta
+ *    and y 16-byte aligned (it returns M3_ERR_ALIGN otherwise).
+ *    The library never allocates device memory and never frees a pointer.
+ *  - Arguments are validated on the host before any launch; on error nothing
+ *    is launched and a negative status is returned.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns before it completes.
+ *  - Device-side errors (a bounded wait that ran out) are recorded in a
+ *    per-device status word; m3_device_status() reads and clears it.
+ *  - Not thread-safe per device for concurrent calls only in that the status
+ *    word is shared; outputs never overlap inputs.
+ */
+#ifndef M3SCAN_H
+#define M3SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define M3_API __attribute__((visibility("default")))
+#else
+#define M3_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, B, C, theta, y (and of x_t, B_t, C_t, theta_t, prev_B,
+ * prev_x, y_t for m3_step).  dt, lambda, A and the state are always fp32. */
+typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
+
+/* Problem sizes.  batch b >= 0, seqlen T >= 0 (ignored by m3_step),
+ * heads h >= 1, headdim P in [4, 256] with P % 4 == 0, dstate N in [2, 256]
+ * even, rank R in [1, 8], chunk Q in {16, 32, 64, 128} (tokens per chunk of
+ * the prefill; the result does not depend on it beyond rounding). */
+typedef struct {
+    int64_t batch;
+    int64_t seqlen;
+    int64_t heads;
+    int64_t headdim;  /* P */
+    int64_t dstate;   /* N */
+    int64_t rank;     /* R, 1 = SISO */
+    int64_t chunk;    /* Q */
+    int32_t dtype;    /* m3_dtype */
+    int32_t reserved; /* must be 0 */
+} m3_dims;
+
+/* Status codes. */
+#define M3_OK 0
+#define M3_ERR_NULL (-1)        /* a required pointer is NULL */
+#define M3_ERR_SHAPE (-2)       /* a size is out of range */
+#define M3_ERR_DTYPE (-3)       /* unknown dtype */
+#define M3_ERR_ALIGN (-4)       /* a pointer is not aligned as required */
+#define M3_ERR_CUDA (-5)        /* a CUDA call or launch failed (no device, ...) */
+#define M3_ERR_UNSUPPORTED (-6) /* valid sizes this build has no kernel for */
+#define M3_ERR_DEVICE (-7)      /* the device status word was set */
+#define M3_ERR_WORKSPACE (-8)   /* workspace too small */
+
+/* Prefill algorithms (what m3_scan_fwd would run for given dims). */
+#define M3_ALGO_NONE (-1)       /* no kernel for these dims */
+#define M3_ALGO_SEQUENTIAL 0    /* fp32 SIMT kernel, one token at a time */
+#define M3_ALGO_CHUNKED_TC 1    /* chunked tcgen05 (tensor core) kernel */
+
+/* Bytes of device workspace m3_scan_fwd needs for `d` (0 for every kernel of
+ * this build).  Returns 0 for invalid dims as well. */
+M3_API size_t m3_scan_workspace_size(const m3_dims* d);
+
+/* Which prefill kernel m3_scan_fwd runs for `d`: M3_ALGO_CHUNKED_TC for bf16
+ * inputs with P == 64, N in {64, 128}, R * Q <= 128 ... (see DESIGN), else
+ * M3_ALGO_SEQUENTIAL; M3_ALGO_NONE for invalid dims. */
+M3_API int m3_scan_algorithm(const m3_dims* d);
+
+/* Chunked prefill from the zero state (Mamba-3 summary page §3.1-§3.3; the
+ * chunked evaluation is the SSD intra-chunk / inter-chunk split of the
+ * Mamba-2 chapter page, "Foundation Model Engineering" ch. 20.2 §2).
+ *   x      [b, T, h, R, P]  dtype
+ *   dt     [b, T, h]        fp32, > 0
+ *   A      [h]              fp32, <= 0
+ *   B, C   [b, T, h, R, N]  dtype
+ *   lambda [b, T, h]        fp32 in [0, 1], or NULL for lambda = 1
+ *   theta  [b, T, h, N/2]   dtype, or NULL for theta = 0
+ *   y      [b, T, h, R, P]  dtype, written
+ *   final_state [b, h, N, P] fp32, written (complex frame), or NULL
+ *   workspace / workspace_bytes: device scratch of at least
+ *          m3_scan_workspace_size(d) bytes (may be NULL when that is 0).
+ * Returns M3_OK or a negative status; T == 0 writes only final_state (zero). */
+M3_API int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A,
+                const void* B, const void* C, const float* lambda, const void* theta,
+                void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* One decode step for every (b, h) (same recurrence, one token):
+ *   state   [b, h, N, P]  fp32, read and overwritten with h'_t (complex frame)
+ *   x_t     [b, h, R, P]  dtype      dt_t, lambda_t [b, h] fp32 (lambda_t may
+ *   B_t,C_t [b, h, R, N]  dtype      be NULL for 1)       A [h] fp32
+ *   theta_t [b, h, N/2]   dtype, the angle of this step (NULL for 0)
+ *   prev_B  [b, h, R, N], prev_x [b, h, R, P]  dtype: the previous token's B
+ *           and x (the beta term's B_{t-1} x_{t-1}^T); both NULL for none.
+ *   y_t     [b, h, R, P]  dtype, written.
+ * d->seqlen and d->chunk are ignored.  The caller keeps (B_t, x_t) as the next
+ * call's (prev_B, prev_x). */
+M3_API int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t,
+            const float* A, const void* B_t, const void* C_t, const float* lambda_t,
+            const void* theta_t, const void* prev_B, const void* prev_x, void* y_t,
+            void* stream);
+
+/* Reads and clears the device status word of the current device after
+ * synchronising `stream`: M3_OK, M3_ERR_DEVICE if a kernel reported a
+ * device-side error since the last call, or M3_ERR_CUDA. */
+M3_API int m3_device_status(void* stream);
+
+/* Static text for a status code. */
+M3_API const char* m3_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3SCAN_H */

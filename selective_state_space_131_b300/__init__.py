@@ -7,15 +7,12 @@ seeded synthetic workloads.  Importing this package does not load the CUDA
 library; importing ``selective_state_space_131_b300.m3scan`` does, and fails
 loudly when it is missing.
 """
+import importlib
 
 __all__ = ["inputs", "m3scan"]
 
 
 def __getattr__(name):
-    if name == "m3scan":
-        from . import m3scan
-        return m3scan
-    if name == "inputs":
-        from . import inputs
-        return inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

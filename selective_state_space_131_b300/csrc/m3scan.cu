@@ -1,0 +1,243 @@
+// m3scan.cu -- the C ABI of libm3scan.so (declared in include/m3scan.h):
+// host-side validation, kernel selection and launch.  Every kernel of the
+// library is compiled in this one translation unit.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "m3scan.h"
+#include "common.cuh"
+#include "step_simt.cuh"
+#include "scan_tc.cuh"
+
+namespace {
+
+using m3::SimtArgs;
+using m3::TokLayout;
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0; }
+bool aligned16(const void* p) { return aligned(p, 16); }
+
+// Validates the sizes shared by both entry points.
+int check_dims(const m3_dims* d, bool need_chunk) {
+    if (!d) return M3_ERR_NULL;
+    if (d->dtype != M3_F32 && d->dtype != M3_BF16) return M3_ERR_DTYPE;
+    if (d->reserved != 0) return M3_ERR_SHAPE;
+    if (d->batch < 0 || d->seqlen < 0 || d->heads < 1) return M3_ERR_SHAPE;
+    if (d->headdim < 4 || d->headdim > 256 || d->headdim % 4 != 0) return M3_ERR_SHAPE;
+    if (d->dstate < 2 || d->dstate > 256 || d->dstate % 2 != 0) return M3_ERR_SHAPE;
+    if (d->rank < 1 || d->rank > 8) return M3_ERR_SHAPE;
+    if (need_chunk && d->chunk != 16 && d->chunk != 32 && d->chunk != 64 && d->chunk != 128)
+        return M3_ERR_SHAPE;
+    if (d->batch * d->heads > INT32_MAX) return M3_ERR_SHAPE;
+    return M3_OK;
+}
+
+// SIMT geometry: NPT row pairs per thread, TK threads along pairs, P/4 along P.
+bool simt_geometry(const m3_dims* d, SimtArgs* a, int* npt, int* block) {
+    const int N = (int)d->dstate, P = (int)d->headdim, R = (int)d->rank;
+    const int K = N / 2, P4 = P / 4, units = K * P4;
+    int n = 1;
+    while (units / n > 256 && K % (2 * n) == 0 && n < 8) n *= 2;
+    if (units / n > 512) return false;
+    a->R = R; a->P = P; a->N = N; a->K = K; a->P4 = P4; a->TK = K / n;
+    *npt = n;
+    *block = a->TK * P4;
+    return true;
+}
+
+size_t step_smem_bytes(const SimtArgs& a) {
+    const TokLayout L(a.R, a.P, a.N);
+    return sizeof(float) * (2 * (size_t)L.size + (size_t)a.TK * a.R * a.P);
+}
+size_t seq_smem_bytes(const SimtArgs& a) {
+    const TokLayout L(a.R, a.P, a.N);
+    return sizeof(float) * (3 * (size_t)L.size + 2 * (size_t)a.TK * a.R * a.P);
+}
+
+template <typename K>
+int prepare(K kernel, size_t smem) {
+    if (smem > kMaxSmem) return M3_ERR_UNSUPPORTED;
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return M3_ERR_CUDA;
+    }
+    return M3_OK;
+}
+
+int launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+template <typename T, int NPT>
+int launch_step(const m3_dims* d, const SimtArgs& a, int block, float* state, const void* x_t, const float* dt_t,
+                const float* A, const void* B_t, const void* C_t, const float* lam_t, const void* theta_t,
+                const void* prev_B, const void* prev_x, void* y_t, cudaStream_t s) {
+    auto k = m3::m3_step_kernel<T, NPT>;
+    const size_t smem = step_smem_bytes(a);
+    int rc = prepare(k, smem);
+    if (rc != M3_OK) return rc;
+    k<<<(unsigned)(d->batch * d->heads), block, smem, s>>>(
+        a, d->heads, state, (const T*)x_t, dt_t, A, (const T*)B_t, (const T*)C_t, lam_t, (const T*)theta_t,
+        (const T*)prev_B, (const T*)prev_x, (T*)y_t);
+    return launch_status();
+}
+
+template <typename T, int NPT>
+int launch_seq(const m3_dims* d, const SimtArgs& a, int block, const void* x, const float* dt, const float* A,
+               const void* B, const void* C, const float* lam, const void* theta, void* y, float* final_state,
+               cudaStream_t s) {
+    auto k = m3::m3_scan_seq_kernel<T, NPT>;
+    const size_t smem = seq_smem_bytes(a);
+    int rc = prepare(k, smem);
+    if (rc != M3_OK) return rc;
+    k<<<(unsigned)(d->batch * d->heads), block, smem, s>>>(a, d->seqlen, d->heads, (const T*)x, dt, A, (const T*)B,
+                                                          (const T*)C, lam, (const T*)theta, (T*)y, final_state);
+    return launch_status();
+}
+
+template <typename T>
+int dispatch_seq(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                 const float* lam, const void* theta, void* y, float* fs, cudaStream_t s) {
+    SimtArgs a;
+    int npt, block;
+    if (!simt_geometry(d, &a, &npt, &block)) return M3_ERR_UNSUPPORTED;
+    switch (npt) {
+        case 1: return launch_seq<T, 1>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
+        case 2: return launch_seq<T, 2>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
+        case 4: return launch_seq<T, 4>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
+        case 8: return launch_seq<T, 8>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
+    }
+    return M3_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+int dispatch_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A,
+                  const void* B_t, const void* C_t, const float* lam_t, const void* theta_t, const void* prev_B,
+                  const void* prev_x, void* y_t, cudaStream_t s) {
+    SimtArgs a;
+    int npt, block;
+    if (!simt_geometry(d, &a, &npt, &block)) return M3_ERR_UNSUPPORTED;
+    switch (npt) {
+        case 1: return launch_step<T, 1>(d, a, block, state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, s);
+        case 2: return launch_step<T, 2>(d, a, block, state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, s);
+        case 4: return launch_step<T, 4>(d, a, block, state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, s);
+        case 8: return launch_step<T, 8>(d, a, block, state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, s);
+    }
+    return M3_ERR_UNSUPPORTED;
+}
+
+int scan_algorithm(const m3_dims* d) {
+    if (check_dims(d, true) != M3_OK) return M3_ALGO_NONE;
+    if (m3tc::supports(*d)) return M3_ALGO_CHUNKED_TC;
+    SimtArgs a;
+    int npt, block;
+    if (!simt_geometry(d, &a, &npt, &block) || seq_smem_bytes(a) > kMaxSmem) return M3_ALGO_NONE;
+    return M3_ALGO_SEQUENTIAL;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t m3_scan_workspace_size(const m3_dims* d) {
+    (void)d;
+    return 0;
+}
+
+int m3_scan_algorithm(const m3_dims* d) { return scan_algorithm(d); }
+
+int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                const float* lambda, const void* theta, void* y, float* final_state, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    int rc = check_dims(d, true);
+    if (rc != M3_OK) return rc;
+    (void)workspace;
+    (void)workspace_bytes;
+    const bool has_tokens = d->batch > 0 && d->seqlen > 0;
+    if (has_tokens && (!x || !dt || !A || !B || !C || !y)) return M3_ERR_NULL;
+    if (d->batch > 0 && !A) return M3_ERR_NULL;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x, B, C, theta, y};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt, A, lambda};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (final_state && !aligned16(final_state)) return M3_ERR_ALIGN;
+    const int algo = scan_algorithm(d);
+    if (algo == M3_ALGO_NONE) return M3_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d->batch == 0) return M3_OK;
+    if (d->seqlen == 0) {
+        if (final_state &&
+            cudaMemsetAsync(final_state, 0, sizeof(float) * d->batch * d->heads * d->dstate * d->headdim, s) !=
+                cudaSuccess)
+            return M3_ERR_CUDA;
+        return M3_OK;
+    }
+    if (algo == M3_ALGO_CHUNKED_TC)
+        return m3tc::launch(*d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+    if (d->dtype == M3_F32)
+        return dispatch_seq<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+    return dispatch_seq<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+}
+
+int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A, const void* B_t,
+            const void* C_t, const float* lambda_t, const void* theta_t, const void* prev_B, const void* prev_x,
+            void* y_t, void* stream) {
+    int rc = check_dims(d, false);
+    if (rc != M3_OK) return rc;
+    if (d->batch > 0 && (!state || !x_t || !dt_t || !A || !B_t || !C_t || !y_t)) return M3_ERR_NULL;
+    if ((prev_B == nullptr) != (prev_x == nullptr)) return M3_ERR_NULL;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x_t, B_t, C_t, theta_t, prev_B, prev_x, y_t};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt_t, A, lambda_t};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (state && !aligned16(state)) return M3_ERR_ALIGN;
+    SimtArgs a;
+    int npt, block;
+    if (!simt_geometry(d, &a, &npt, &block) || step_smem_bytes(a) > kMaxSmem) return M3_ERR_UNSUPPORTED;
+    if (d->batch == 0) return M3_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d->dtype == M3_F32)
+        return dispatch_step<float>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x, y_t, s);
+    return dispatch_step<__nv_bfloat16>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x, y_t,
+                                        s);
+}
+
+int m3_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return M3_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, m3::g_status, sizeof(v)) != cudaSuccess) return M3_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(m3::g_status, &zero, sizeof(zero)) != cudaSuccess) return M3_ERR_CUDA;
+        return M3_ERR_DEVICE;
+    }
+    return M3_OK;
+}
+
+const char* m3_status_string(int status) {
+    switch (status) {
+        case M3_OK: return "ok";
+        case M3_ERR_NULL: return "a required pointer is NULL";
+        case M3_ERR_SHAPE: return "a size is out of range";
+        case M3_ERR_DTYPE: return "unknown dtype";
+        case M3_ERR_ALIGN: return "a pointer is not aligned as required";
+        case M3_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case M3_ERR_UNSUPPORTED: return "no kernel for these sizes";
+        case M3_ERR_DEVICE: return "a kernel reported a device-side error";
+        case M3_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

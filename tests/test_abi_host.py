@@ -1,0 +1,109 @@
+"""The C-ABI library on the host: it loads, exports every entry point the
+header declares, and rejects bad arguments before any launch.  No kernel
+runs here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_131_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m3():
+    if not build.up_to_date():
+        build.build()
+    from selective_state_space_131_b300 import m3scan
+    return m3scan
+
+
+def declared_symbols():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names += re.findall(r"M3_API[^;(]*?\b(m3_\w+)\s*\(", src)
+    return names
+
+
+def test_every_declared_symbol_is_exported(m3):
+    names = declared_symbols()
+    assert {"m3_scan_fwd", "m3_step", "m3_scan_workspace_size", "m3_status_string"} <= set(names)
+    lib = ctypes.CDLL(m3.LIBRARY_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(m3):
+    for code in range(-8, 1):
+        assert m3.m3_status_string(code) != "unknown status"
+    assert m3.m3_status_string(-99) == "unknown status"
+
+
+def _dims(m3, **kw):
+    base = dict(batch=2, seqlen=100, heads=4, headdim=64, dstate=64, rank=1, chunk=64, dtype=m3.M3_BF16)
+    base.update(kw)
+    return m3.make_dims(**base)
+
+
+FAKE = 0x7f0000000000  # never dereferenced: every call below fails validation first
+
+
+def _scan_ptrs(**over):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, lam=FAKE, theta=FAKE, y=FAKE, fs=FAKE, ws=None, wsb=0)
+    p.update(over)
+    return [p[k] for k in ("x", "dt", "A", "B", "C", "lam", "theta", "y", "fs", "ws", "wsb")]
+
+
+def test_scan_validation(m3):
+    assert m3.raw_scan_fwd(_dims(m3), _scan_ptrs(x=None)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_fwd(_dims(m3), _scan_ptrs(C=None)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_fwd(_dims(m3, dstate=63), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, headdim=62), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, rank=9), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, chunk=48), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, heads=0), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, seqlen=-1), _scan_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd(_dims(m3, dtype=7), _scan_ptrs()) == m3.M3_ERR_DTYPE
+    assert m3.raw_scan_fwd(_dims(m3), _scan_ptrs(y=FAKE + 1)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd(_dims(m3, dtype=m3.M3_F32), _scan_ptrs(theta=FAKE + 2)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd(_dims(m3), _scan_ptrs(dt=FAKE + 2)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd(_dims(m3), _scan_ptrs(fs=FAKE + 8)) == m3.M3_ERR_ALIGN
+    d = _dims(m3)
+    d.reserved = 1
+    assert m3.raw_scan_fwd(d, _scan_ptrs()) == m3.M3_ERR_SHAPE
+    # an empty batch is valid and launches nothing
+    assert m3.raw_scan_fwd(_dims(m3, batch=0), _scan_ptrs(x=None, y=None)) == m3.M3_OK
+
+
+def _step_ptrs(**over):
+    p = dict(state=FAKE, x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, lam=FAKE, theta=FAKE, pB=FAKE, px=FAKE, y=FAKE)
+    p.update(over)
+    return [p[k] for k in ("state", "x", "dt", "A", "B", "C", "lam", "theta", "pB", "px", "y")]
+
+
+def test_step_validation(m3):
+    assert m3.raw_step(_dims(m3), _step_ptrs(state=None)) == m3.M3_ERR_NULL
+    assert m3.raw_step(_dims(m3), _step_ptrs(pB=None)) == m3.M3_ERR_NULL    # prev_B and prev_x go together
+    assert m3.raw_step(_dims(m3, dstate=5), _step_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_step(_dims(m3), _step_ptrs(px=FAKE + 1)) == m3.M3_ERR_ALIGN
+    assert m3.raw_step(_dims(m3), _step_ptrs(state=FAKE + 4)) == m3.M3_ERR_ALIGN
+    assert m3.raw_step(_dims(m3, batch=0), _step_ptrs()) == m3.M3_OK
+
+
+def test_algorithm_selection(m3):
+    assert m3.m3_scan_algorithm(_dims(m3, dstate=63)) == m3.M3_ALGO_NONE
+    assert m3.m3_scan_algorithm(_dims(m3, dtype=m3.M3_F32)) == m3.M3_ALGO_SEQUENTIAL
+    assert m3.m3_scan_workspace_size(_dims(m3)) == 0
+
+
+def test_launch_without_gpu_reports_cuda_error(m3):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: fake pointers must not reach a kernel")
+    assert m3.raw_scan_fwd(_dims(m3, dtype=m3.M3_F32), _scan_ptrs()) == m3.M3_ERR_CUDA
+    assert m3.raw_step(_dims(m3), _step_ptrs()) == m3.M3_ERR_CUDA
