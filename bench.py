@@ -1,0 +1,383 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba-3 scan on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1|2|3] [--no-decode] [--no-cpu-baseline]
+
+One step = one chunked prefill (m3_scan_fwd) over one batch of the workload,
+inputs resident in HBM (1.2 GB for the default workload, larger than the
+126 MB L2, so no flush is needed between steps).  Prints ONE JSON line with
+prefill tokens/s (tokens = batch * seqlen) as the headline, the roofline of
+the prefill kernel against the measured HBM copy bandwidth, an end-to-end
+figure through host buffers, the oracle timed on the host cores, and the
+decode sweep (m3_step, steps/s and GB/s) measured in the same run.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (the
+(batch, head) sequences are independent: weak scaling, no collective on the
+data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_131_b300 import inputs  # noqa: E402
+
+HBM_FALLBACK_GBS = 6400.0
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": HBM_FALLBACK_GBS}, "fallback"
+
+
+def scan_bytes(shape: inputs.ScanShape) -> int:
+    """Algorithmic bytes of one prefill: every input read once, y and the
+    final state written once."""
+    b, T, H, P, N, R = shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.rank
+    es = 2 if shape.dtype == "bf16" else 4
+    tok = b * T * H
+    n = tok * R * P * es * 2            # x read, y written
+    n += tok * R * N * es * 2           # B, C
+    n += tok * 4                        # dt
+    n += tok * 4 if shape.with_lambda else 0
+    n += tok * (N // 2) * es if shape.with_theta else 0
+    n += H * 4                          # A
+    n += b * H * N * P * 4              # final state
+    return n
+
+
+def scan_flops(shape: inputs.ScanShape) -> int:
+    """The chunked algorithm's flop count per token and head, R [2Q(N+P) + 4NP]."""
+    b, T, H, P, N, R, Q = (shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.rank,
+                           shape.chunk)
+    return b * T * H * R * (2 * Q * (N + P) + 4 * N * P)
+
+
+def decode_bytes(shape: inputs.DecodeShape) -> int:
+    """Algorithmic bytes of one decode step: state read + written, inputs read
+    (x, B, C, theta, dt, lambda, prev B, prev x), y written."""
+    b, H, P, N, R = shape.batch, shape.heads, shape.headdim, shape.dstate, shape.rank
+    es = 2 if shape.dtype == "bf16" else 4
+    u = b * H
+    return u * (2 * N * P * 4 + R * P * es * 3 + R * N * es * 3 + (N // 2) * es + 8)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        sm = sorted(r[0] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0][1], "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(shape: inputs.ScanShape, seed: int, units: int):
+    """Inputs of `units` sequences (batch row 0, heads 0..units-1) of the workload."""
+    inp = inputs.make_scan_inputs(inputs.ScanShape(**{**shape.__dict__, "batch": 1}), seed)
+    hs = list(range(min(units, shape.heads)))
+    return {k: (None if v is None else (v[hs] if k == "A" else v[:, :, hs])) for k, v in inp.items()}, len(hs)
+
+
+def time_cpu_oracle(shape: inputs.ScanShape, sample, n_units: int):
+    """The fp64 oracle (as it stands) on a sample of sequences: returns
+    (tokens/s equivalent, seconds, threads).  A token is one position of one
+    batch row across all heads, so `n_units` sequences count n_units/heads."""
+    import oracle
+    nthreads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.scan(sample["x"], sample["dt"], sample["A"], sample["B"], sample["C"], sample["lam"],
+                sample["theta"], nthreads=nthreads)
+    sec = time.perf_counter() - t0
+    tokens = shape.seqlen * n_units / shape.heads
+    return tokens / sec, sec, nthreads
+
+
+def run_reference(args, shape, cfg_name):
+    """--impl reference: the oracle on the host cores, a bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    # size each step's sample so that warm-up + steps fit the wall budget
+    full, _ = oracle_sample(shape, args.workload, args.ref_units)
+    one = {k: (None if v is None else (v[:1] if k == "A" else v[:, :, :1])) for k, v in full.items()}
+    _, sec1, thr = time_cpu_oracle(shape, one, 1)
+    n_steps = args.warmup + args.steps
+    units = int(max(1, min(args.ref_units, args.ref_budget_s / max(n_steps, 1) / sec1 * thr)))
+    sample = {k: (None if v is None else (v[:units] if k == "A" else v[:, :, :units])) for k, v in full.items()}
+    vals = []
+    for i in range(n_steps):
+        tps, sec, thr = time_cpu_oracle(shape, sample, units)
+        if i >= args.warmup:
+            vals.append((tps, sec))
+    tps = sum(v[0] for v in vals) / len(vals)
+    sec = sum(v[1] for v in vals) / len(vals)
+    sample = f"batch row 0, heads 0..{units - 1} of {cfg_name}, full T={shape.seqlen} (each step)"
+    return {
+        "impl": "reference", "metric": "prefill_tokens_per_s", "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, the pages' distributions)",
+        "config": {"workload": cfg_name, **{k: v for k, v in shape.__dict__.items()}},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def bench_decode(m3, stream, steps: int, rank_seed: int):
+    """Decode sweep of the decode workload (SISO): `steps` consecutive m3_step
+    calls captured in one CUDA graph; returns a dict."""
+    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": steps})
+    inp = inputs.make_decode_inputs(shape, 4 + rank_seed, device="cuda")
+    state = inp["state0"].clone()
+    ys = torch.empty_like(inp["x"][1:])
+    dims = m3.step_dims(inp["x"][0], inp["B"][0])
+
+    def sweep():
+        for s in range(steps):
+            m3.m3_step(state, inp["x"][s + 1], inp["dt"][s + 1], inp["A"], inp["B"][s + 1], inp["C"][s + 1],
+                       inp["lam"][s + 1], inp["theta"][s + 1], inp["B"][s], inp["x"][s], ys[s], stream=stream,
+                       dims=dims)
+    with torch.cuda.stream(stream):
+        sweep()                      # warm-up (also the first sweep of the state)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * steps)
+    nbytes = decode_bytes(shape)
+    del inp, ys, state, g
+    torch.cuda.empty_cache()
+    return {"workload": inputs.CONFIG_NAMES[4] + "_R1", "steps_per_s": 1e3 / ms, "us_per_step": ms * 1e3,
+            "tokens_per_s": shape.batch * 1e3 / ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9,
+            "bytes_per_step": nbytes, "graph_steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-units", type=int, default=32, help="sequences in the oracle sample (cpu_baseline)")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0, help="wall budget of the reference arm")
+    ap.add_argument("--decode-steps", type=int, default=1024)
+    args = ap.parse_args()
+
+    shape = inputs.CONFIGS[args.workload]
+    cfg_name = inputs.CONFIG_NAMES[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        out = run_reference(args, shape, cfg_name)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    from selective_state_space_131_b300 import m3scan as m3
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream()
+
+    inp = inputs.make_scan_inputs(shape, args.workload + 1000 * rank)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    b, T, H, R, P = d["x"].shape
+    N = d["B"].shape[-1]
+    y = torch.empty_like(d["x"])
+    fs = torch.empty(b, H, N, P, device=dev, dtype=torch.float32)
+    dims = m3.scan_dims(d["x"], d["B"], shape.chunk)
+    algo = m3.m3_scan_algorithm(dims)
+
+    def step():
+        m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], y, fs, stream=stream,
+                       dims=dims)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set during the timed region")
+
+    tokens = b * T
+    value = world * tokens / (ms * 1e-3)
+    peaks, peak_kind = measured_peaks()
+    nbytes = scan_bytes(shape)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    result = {
+        "metric": "prefill_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if shape.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded, the pages' input distributions; no dataset)",
+        "config": {"workload": cfg_name, "batch": b, "seqlen": T, "heads": H, "headdim": P, "dstate": N,
+                   "rank": R, "chunk": shape.chunk, "lambda": shape.with_lambda, "theta": shape.with_theta,
+                   "l2": "inputs (%.2f GB) larger than L2; no flush" % (nbytes / 1e9),
+                   "algorithm": {0: "sequential_simt", 1: "chunked_tcgen05"}.get(algo, str(algo)),
+                   "parallelism": f"weak x{world} (independent sequences per rank)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "algorithmic_bytes": nbytes,
+                     "tensor_tflops": scan_flops(shape) / (ms * 1e-3) / 1e12},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        # end to end through the public API with host buffers: pinned host -> device
+        # copies of the step's inputs, the prefill, device -> host copy of y.
+        host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = y_host.numel() * y_host.element_size()
+        e_steps = max(3, min(20, args.steps // 20))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    if v is not None:
+                        d[k].copy_(v, non_blocking=True)
+                step()
+                y_host.copy_(y, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        a1.record(stream)
+        barrier()
+        ems = a0.elapsed_time(a1) / e_steps
+        result["e2e"] = {"value": world * tokens / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": e_steps}
+
+    if not args.no_decode and rank == 0:
+        del d, y, fs
+        torch.cuda.empty_cache()
+        dec = bench_decode(m3, stream, args.decode_steps, rank)
+        dec["roofline_frac"] = dec["GB_per_s"] / peaks["hbm_gbs"]
+        result["decode"] = dec
+
+    if not args.no_cpu_baseline and rank == 0:
+        sample, nu = oracle_sample(shape, args.workload, args.ref_units)
+        tps, sec, thr = time_cpu_oracle(shape, sample, nu)
+        result["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                  "sample": f"batch row 0, heads 0..{args.ref_units - 1}, full T={T} "
+                                            f"({sec:.1f} s)"}
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,129 @@
+"""GPU parity of the chunked tensor-core prefill (M3_ALGO_CHUNKED_TC) against
+the fp64 oracle: small shapes spanning several chunks and a ragged tail, the
+three bf16 workloads at full size on sampled (batch, head) sequences, chunk
+invariance, prefill -> decode continuation and determinism."""
+import numpy as np
+import pytest
+import torch
+
+from selective_state_space_131_b300 import inputs
+from tests.gpu_util import TOL, dev, gpu_scan, max_rel, oracle_scan, sub_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m3():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from selective_state_space_131_b300 import m3scan
+    return m3scan
+
+
+def run_and_check(m3, shape, seed, bsel=None, hsel=None, tol=None):
+    inp = inputs.make_scan_inputs(shape, seed)
+    dims = m3.scan_dims(inp["x"], inp["B"], shape.chunk)
+    assert m3.m3_scan_algorithm(dims) == m3.M3_ALGO_CHUNKED_TC
+    y, fs = gpu_scan(m3, dev(inp), shape.chunk)
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+    y, fs = y.float().cpu(), fs.cpu()
+    if bsel is not None:
+        y = y[bsel][:, :, hsel]
+        fs = fs[bsel][:, hsel]
+    yr, fr = oracle_scan(inp, bsel, hsel)
+    ey, ef = max_rel(y, yr), max_rel(fs, fr)
+    tol = tol or TOL[shape.dtype]
+    assert np.isfinite(ey) and np.isfinite(ef)
+    assert ey <= tol and ef <= tol, (ey, ef)
+    return ey, ef
+
+
+SMALL = [
+    # (T, N, R, chunk, lambda, theta)
+    (209, 64, 1, 64, True, True),
+    (209, 64, 1, 128, True, True),
+    (64, 64, 1, 64, True, True),
+    (1, 64, 1, 64, True, True),
+    (37, 64, 1, 64, True, True),
+    (209, 128, 1, 64, True, True),
+    (209, 128, 1, 64, False, False),
+    (209, 64, 1, 64, False, False),
+    (130, 64, 2, 64, True, True),
+    (130, 64, 4, 64, True, True),
+    (130, 64, 4, 16, True, True),
+    (130, 128, 2, 32, True, True),
+    (130, 128, 4, 64, True, False),
+]
+
+
+@pytest.mark.parametrize("T,N,R,chunk,lam,th", SMALL,
+                         ids=lambda v: str(v))
+def test_tc_small(m3, T, N, R, chunk, lam, th):
+    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=N, rank=R, chunk=chunk, dtype="bf16",
+                             with_lambda=lam, with_theta=th)
+    ey, ef = run_and_check(m3, shape, 1000 + T + N + R)
+    print(f"T{T} N{N} R{R} Q{chunk} lam{lam} th{th}: y {ey:.2e} state {ef:.2e}")
+
+
+BSEL = [0, 7]
+HSEL = [0, 13, 31]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+def test_tc_full_size_workloads(m3, cfg):
+    """The bf16 workloads at full size (the bench's launch configuration), checked
+    on sampled (batch, head) sequences the oracle computes exactly."""
+    shape = inputs.CONFIGS[cfg]
+    ey, ef = run_and_check(m3, shape, cfg, BSEL, HSEL)
+    print(f"config {cfg}: y {ey:.2e} state {ef:.2e}")
+
+
+def test_chunk_invariance(m3):
+    """The result does not depend on the chunk size beyond rounding."""
+    shape = inputs.ScanShape(batch=2, seqlen=300, heads=2, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16")
+    d = dev(inputs.make_scan_inputs(shape, 5))
+    y64, f64 = gpu_scan(m3, d, 64)
+    y128, f128 = gpu_scan(m3, d, 128)
+    torch.cuda.synchronize()
+    assert max_rel(y64.float().cpu(), y128.float().cpu()) <= 2e-2
+    assert max_rel(f64.cpu(), f128.cpu()) <= 2e-2
+
+
+def test_tc_prefill_then_decode(m3):
+    """Prefill (tensor cores) then bf16 decode steps continue the same sequence."""
+    shape = inputs.ScanShape(batch=2, seqlen=150, heads=2, headdim=64, dstate=64, rank=2, chunk=64, dtype="bf16")
+    inp = inputs.make_scan_inputs(shape, 23)
+    d = dev(inp)
+    T0 = 140
+    pre = {k: (v[:, :T0].contiguous() if (v is not None and k != "A") else v) for k, v in d.items()}
+    y0, state = gpu_scan(m3, pre, 64)
+    ys = [y0.float()]
+    for t in range(T0, 150):
+        y = torch.empty_like(d["x"][:, t])
+        m3.m3_step(state, d["x"][:, t].contiguous(), d["dt"][:, t].contiguous(), d["A"], d["B"][:, t].contiguous(),
+                   d["C"][:, t].contiguous(), d["lam"][:, t].contiguous(), d["theta"][:, t].contiguous(),
+                   d["B"][:, t - 1].contiguous(), d["x"][:, t - 1].contiguous(), y)
+        ys.append(y[:, None].float())
+    torch.cuda.synchronize()
+    yr, fr = oracle_scan(inp)
+    assert max_rel(torch.cat(ys, 1).cpu(), yr) <= 2e-2
+    assert max_rel(state.cpu(), fr) <= 2e-2
+
+
+def test_tc_deterministic(m3):
+    shape = inputs.ScanShape(batch=2, seqlen=257, heads=2, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16")
+    d = dev(inputs.make_scan_inputs(shape, 6))
+    y1, f1 = gpu_scan(m3, d, 64)
+    y2, f2 = gpu_scan(m3, d, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
+
+
+def test_tc_without_final_state(m3):
+    shape = inputs.ScanShape(batch=1, seqlen=100, heads=2, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16")
+    inp = inputs.make_scan_inputs(shape, 8)
+    y, _ = gpu_scan(m3, dev(inp), 64, with_state=False)
+    torch.cuda.synchronize()
+    yr, _ = oracle_scan(inp)
+    assert max_rel(y.float().cpu(), yr) <= 2e-2
