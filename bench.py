@@ -35,6 +35,31 @@ from selective_state_space_131_b300 import inputs  # noqa: E402
 
 HBM_FALLBACK_GBS = 6400.0
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# prefill kernel from one ncu capture, keyed by workload, with the sha256 prefix
+# of the kernel source the counters were taken on: reported only while the
+# source is unchanged, else null.  Captured on batch 2 and scaled x4 to batch 8
+# (traffic grows with the number of (batch, head) sequences); the summary with
+# its command is profiles/m3_scan_tc_siso_b2T8192P64N64.md.
+NCU_TRAFFIC = {
+    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.131392e6 + 51.497984e6),
+                                      "source": "selective_state_space_131_b300/csrc/scan_tc.cuh",
+                                      "sha256": "81ee047a047b5f20"},
+}
+
+
+def ncu_traffic(workload: str):
+    import hashlib
+    rec = NCU_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    try:
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return rec["bytes"] if sha.startswith(rec["sha256"]) else None
+
 
 def measured_peaks():
     try:
@@ -189,10 +214,11 @@ def run_reference(args, shape, cfg_name):
     }
 
 
-def bench_decode(m3, stream, steps: int, rank_seed: int):
-    """Decode sweep of the decode workload (SISO): `steps` consecutive m3_step
-    calls captured in one CUDA graph; returns a dict."""
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": steps})
+def bench_decode(m3, stream, steps: int, rank_seed: int, rank: int = 1):
+    """Decode sweep of the decode workload (fp32, b256 h32 P64 N64, rank R):
+    `steps` consecutive m3_step calls captured in one CUDA graph and replayed
+    on `stream` (the stream the events are recorded on); returns a dict."""
+    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": steps, "rank": rank})
     inp = inputs.make_decode_inputs(shape, 4 + rank_seed, device="cuda")
     state = inp["state0"].clone()
     ys = torch.empty_like(inp["x"][1:])
@@ -203,6 +229,7 @@ def bench_decode(m3, stream, steps: int, rank_seed: int):
             m3.m3_step(state, inp["x"][s + 1], inp["dt"][s + 1], inp["A"], inp["B"][s + 1], inp["C"][s + 1],
                        inp["lam"][s + 1], inp["theta"][s + 1], inp["B"][s], inp["x"][s], ys[s], stream=stream,
                        dims=dims)
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         sweep()                      # warm-up (also the first sweep of the state)
     torch.cuda.synchronize()
@@ -210,22 +237,52 @@ def bench_decode(m3, stream, steps: int, rank_seed: int):
     with torch.cuda.graph(g, stream=stream):
         sweep()
     torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = 3
-    e0.record(stream)
-    for _ in range(reps):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()                   # warm replay
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set during the decode sweep")
     ms = e0.elapsed_time(e1) / (reps * steps)
     nbytes = decode_bytes(shape)
     del inp, ys, state, g
     torch.cuda.empty_cache()
-    return {"workload": inputs.CONFIG_NAMES[4] + "_R1", "steps_per_s": 1e3 / ms, "us_per_step": ms * 1e3,
+    return {"workload": inputs.CONFIG_NAMES[4] + f"_R{rank}", "steps_per_s": 1e3 / ms, "us_per_step": ms * 1e3,
             "tokens_per_s": shape.batch * 1e3 / ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9,
-            "bytes_per_step": nbytes, "graph_steps": steps}
+            "bytes_per_step": nbytes, "graph_steps": steps, "launches_per_step": 1}
+
+
+def time_prefill(m3, stream, shape, seed, dev, steps, warmup):
+    """Device time (ms) of one prefill of `shape` on resident inputs, CUDA
+    events on `stream` around `steps` back-to-back launches."""
+    inp = inputs.make_scan_inputs(shape, seed)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    b, T, H, R, P = d["x"].shape
+    y = torch.empty_like(d["x"])
+    fs = torch.empty(b, H, d["B"].shape[-1], P, device=dev, dtype=torch.float32)
+    dims = m3.scan_dims(d["x"], d["B"], shape.chunk)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], y, fs, stream=stream,
+                           dims=dims)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            m3.m3_scan_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], y, fs, stream=stream,
+                           dims=dims)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set")
+    ms = e0.elapsed_time(e1) / steps
+    del d, y, fs
+    torch.cuda.empty_cache()
+    return ms
 
 
 def main():
@@ -241,9 +298,14 @@ def main():
     ap.add_argument("--ref-units", type=int, default=32, help="sequences in the oracle sample (cpu_baseline)")
     ap.add_argument("--ref-budget-s", type=float, default=150.0, help="wall budget of the reference arm")
     ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
+    ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--decode-only", action="store_true", help="only the decode sweep (profiling captures)")
     args = ap.parse_args()
 
     shape = inputs.CONFIGS[args.workload]
+    if args.batch:
+        shape = inputs.ScanShape(**{**shape.__dict__, "batch": args.batch})
     cfg_name = inputs.CONFIG_NAMES[args.workload]
     world, rank, local = dist_env()
 
@@ -260,6 +322,10 @@ def main():
     from selective_state_space_131_b300 import m3scan as m3
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream()
+    if args.decode_only:
+        for r in (1, 4):
+            print(json.dumps(bench_decode(m3, stream, args.decode_steps, rank, rank=r)), flush=True)
+        return 0
 
     inp = inputs.make_scan_inputs(shape, args.workload + 1000 * rank)
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
@@ -320,7 +386,8 @@ def main():
                    "algorithm": {0: "sequential_simt", 1: "chunked_tcgen05"}.get(algo, str(algo)),
                    "parallelism": f"weak x{world} (independent sequences per rank)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": (ncu_traffic(cfg_name) if not args.batch else None),
                      "peak_kind": f"{peak_kind} HBM copy bandwidth", "algorithmic_bytes": nbytes,
                      "tensor_tflops": scan_flops(shape) / (ms * 1e-3) / 1e12},
         "gpu_launches": args.steps,
@@ -356,11 +423,29 @@ def main():
         result["e2e"] = {"value": world * tokens / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": e_steps}
 
+    del d, y, fs
+    torch.cuda.empty_cache()
+    if not args.no_other and rank == 0:
+        # the other prefill workloads, same protocol (reported beside the headline)
+        other = {}
+        for w in (1, 2, 3):
+            if w == args.workload:
+                continue
+            sh = inputs.CONFIGS[w]
+            wms = time_prefill(m3, stream, sh, w, dev, steps=20, warmup=3)
+            wb = scan_bytes(sh)
+            other[inputs.CONFIG_NAMES[w]] = {
+                "ms_per_step": wms, "tokens_per_s": sh.batch * sh.seqlen / (wms * 1e-3),
+                "GB_per_s": wb / (wms * 1e-3) / 1e9, "hbm_frac": wb / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "algorithmic_bytes": wb, "tensor_tflops": scan_flops(sh) / (wms * 1e-3) / 1e12}
+        result["other_prefill"] = other
+
     if not args.no_decode and rank == 0:
-        del d, y, fs
-        torch.cuda.empty_cache()
-        dec = bench_decode(m3, stream, args.decode_steps, rank)
-        dec["roofline_frac"] = dec["GB_per_s"] / peaks["hbm_gbs"]
+        dec = {}
+        for r in (1, 4):
+            dr = bench_decode(m3, stream, args.decode_steps, rank, rank=r)
+            dr["roofline_frac"] = dr["GB_per_s"] / peaks["hbm_gbs"]
+            dec[f"R{r}"] = dr
         result["decode"] = dec
 
     if not args.no_cpu_baseline and rank == 0:
