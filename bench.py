@@ -43,7 +43,7 @@ HBM_FALLBACK_GBS = 6400.0
 # its command is profiles/m3_scan_tc_siso_b2T8192P64N64.md.
 NCU_TRAFFIC = {
     "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.131392e6 + 51.497984e6),
-                                      "source": "selective_state_space_131_b300/csrc/scan_tc.cuh",
+                                      "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
                                       "sha256": "81ee047a047b5f20"},
 }
 

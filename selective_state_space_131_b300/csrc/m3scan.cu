@@ -9,7 +9,7 @@
 #include "m3scan.h"
 #include "common.cuh"
 #include "step_simt.cuh"
-#include "scan_tc.cuh"
+#include "scan_ws.cuh"
 
 namespace {
 
@@ -133,7 +133,7 @@ int dispatch_step(const m3_dims* d, float* state, const void* x_t, const float* 
 
 int scan_algorithm(const m3_dims* d) {
     if (check_dims(d, true) != M3_OK) return M3_ALGO_NONE;
-    if (m3tc::supports(*d)) return M3_ALGO_CHUNKED_TC;
+    if (m3ws::supports(*d)) return M3_ALGO_CHUNKED_TC;
     SimtArgs a;
     int npt, block;
     if (!simt_geometry(d, &a, &npt, &block) || seq_smem_bytes(a) > kMaxSmem) return M3_ALGO_NONE;
@@ -181,7 +181,7 @@ int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A
         return M3_OK;
     }
     if (algo == M3_ALGO_CHUNKED_TC)
-        return m3tc::launch(*d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+        return m3ws::launch(*d, x, dt, A, B, C, lambda, theta, y, final_state, s);
     if (d->dtype == M3_F32)
         return dispatch_seq<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);
     return dispatch_seq<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);

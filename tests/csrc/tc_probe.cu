@@ -30,8 +30,8 @@ __device__ uint8_t* align1024(uint8_t* p) {
     return p + ((1024u - (s & 1023u)) & 1023u);
 }
 
-__global__ void umma_probe_kernel(int M, int N, int K, int a_mn, int b_mn, const __nv_bfloat16* A,
-                                  const __nv_bfloat16* B, float* D, unsigned* status) {
+__global__ void umma_probe_kernel(int M, int N, int K, int a_mn, int b_mn, int half_split,
+                                  const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, unsigned* status) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ uint64_t bar;
@@ -79,12 +79,22 @@ __global__ void umma_probe_kernel(int M, int N, int K, int a_mn, int b_mn, const
     const bool ok = ptx::mbar_wait(&bar, 0, 2000000000LL);
     if (!ok && lane == 0) atomicOr(status, 1u);
     ptx::tc_fence_after();
-    if (ok) {
+    if (ok && !half_split) {
         for (int c = 0; c < N; c += 16) {
             uint32_t v[16];
             ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
             ptx::tmem_ld_wait();
             for (int j = 0; j < 16; ++j) D[(size_t)(warp * 32 + lane) * N + c + j] = __uint_as_float(v[j]);
+        }
+    } else if (ok) {
+        // 16x32bx2: thread t < 16 -> lane t, columns [c, c+32); t >= 16 -> lane t-16, [c+32, c+64).
+        // Written to D row (16 * warp + t % 16) of an M-row image.
+        for (int c = 0; c < N; c += 64) {
+            uint32_t v[32];
+            ptx::tmem_ld16x2_32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+            ptx::tmem_ld_wait();
+            const int row = warp * 16 + (lane & 15), c0 = c + (lane >> 4) * 32;
+            for (int j = 0; j < 32; ++j) D[(size_t)row * N + c0 + j] = __uint_as_float(v[j]);
         }
     }
     ptx::tc_fence_before();
@@ -119,16 +129,18 @@ __global__ void tma_probe_kernel(const __grid_constant__ CUtensorMap map, int ro
 
 extern "C" {
 
-// D[128][N] <- TMEM lanes x columns after D = A[M][K] * B[N][K]^T.
+// D[128][N] <- TMEM lanes x columns after D = A[M][K] * B[N][K]^T; with
+// half_split (M = 64 only) D[64][N] <- the rows read with the 16x32bx2 shape.
 // M in {64, 128}, N in {64, 128, 256}, K in {64, 128}; MN-major needs
 // M (or N) a multiple of 64.  Returns a cudaError_t, or -1 for bad sizes.
-__attribute__((visibility("default"))) int probe_umma(int M, int N, int K, int a_mn, int b_mn,
+__attribute__((visibility("default"))) int probe_umma(int M, int N, int K, int a_mn, int b_mn, int half_split,
                                                       const void* A, const void* B, float* D,
                                                       unsigned* status) {
     if (!(M == 64 || M == 128) || !(N == 64 || N == 128 || N == 256) || !(K == 64 || K == 128)) return -1;
+    if (half_split && M != 64) return -1;
     const size_t smem = (size_t)(M + N) * K * 2 + 1024;
     cudaFuncSetAttribute(umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    umma_probe_kernel<<<1, kThreads, smem>>>(M, N, K, a_mn, b_mn, (const __nv_bfloat16*)A,
+    umma_probe_kernel<<<1, kThreads, smem>>>(M, N, K, a_mn, b_mn, half_split, (const __nv_bfloat16*)A,
                                              (const __nv_bfloat16*)B, D, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;

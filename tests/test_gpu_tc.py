@@ -40,20 +40,28 @@ def run_and_check(m3, shape, seed, bsel=None, hsel=None, tol=None):
 
 
 SMALL = [
-    # (T, N, R, chunk, lambda, theta)
+    # (T, N, R, chunk, lambda, theta): several chunks, ragged tails, one token,
+    # exactly one chunk, every (N, R) the tensor-core kernel takes, with and
+    # without lambda / theta
     (209, 64, 1, 64, True, True),
     (209, 64, 1, 128, True, True),
     (64, 64, 1, 64, True, True),
+    (65, 64, 1, 64, True, True),
     (1, 64, 1, 64, True, True),
     (37, 64, 1, 64, True, True),
     (209, 128, 1, 64, True, True),
     (209, 128, 1, 64, False, False),
     (209, 64, 1, 64, False, False),
+    (209, 64, 1, 64, True, False),
+    (209, 64, 1, 64, False, True),
     (130, 64, 2, 64, True, True),
     (130, 64, 4, 64, True, True),
     (130, 64, 4, 16, True, True),
+    (17, 64, 4, 16, True, True),
     (130, 128, 2, 32, True, True),
     (130, 128, 4, 64, True, False),
+    (130, 128, 4, 64, True, True),
+    (513, 64, 1, 64, True, True),
 ]
 
 

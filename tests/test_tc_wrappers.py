@@ -30,12 +30,12 @@ def probe():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     lib = ctypes.CDLL(build_probe())
-    lib.probe_umma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 4
+    lib.probe_umma.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p] * 4
     lib.probe_tma.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 2
     return lib
 
 
-def run_umma(lib, M, N, K, a_mn, b_mn, seed=0):
+def run_umma(lib, M, N, K, a_mn, b_mn, seed=0, half_split=0):
     import torch
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
@@ -43,7 +43,8 @@ def run_umma(lib, M, N, K, a_mn, b_mn, seed=0):
     dA, dB = A.cuda(), B.cuda()
     D = torch.full((128, N), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = lib.probe_umma(M, N, K, a_mn, b_mn, dA.data_ptr(), dB.data_ptr(), D.data_ptr(), st.data_ptr())
+    rc = lib.probe_umma(M, N, K, a_mn, b_mn, half_split, dA.data_ptr(), dB.data_ptr(), D.data_ptr(),
+                        st.data_ptr())
     assert rc == 0, rc
     assert int(st.item()) == 0, "mbarrier wait timed out"
     ref = A.double().numpy() @ B.double().numpy().T
@@ -99,3 +100,14 @@ def test_tma_sw128(probe, rows, c1, c2):
                 chunk = (col // 8) ^ (r % 8)
                 exp[r, chunk * 8 + col % 8] = bits[c2, c1 + r, col]
     assert np.array_equal(img, exp)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N", [64, 128])
+def test_tmem_ld_16x32bx2(probe, N):
+    """The 16x32bx2 TMEM load spreads an M = 64 accumulator over all 32
+    threads of a warp: thread t < 16 gets row 16w + t, columns [c, c+32);
+    thread t >= 16 the same row, columns [c+32, c+64)."""
+    D, ref = run_umma(probe, 64, N, 64, 0, 1, seed=5, half_split=1)
+    err = np.abs(D[:64] - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
