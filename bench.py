@@ -299,13 +299,15 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=150.0, help="wall budget of the reference arm")
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
+    ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen (profiling captures)")
     ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--decode-only", action="store_true", help="only the decode sweep (profiling captures)")
     args = ap.parse_args()
 
     shape = inputs.CONFIGS[args.workload]
-    if args.batch:
-        shape = inputs.ScanShape(**{**shape.__dict__, "batch": args.batch})
+    if args.batch or args.seqlen:
+        shape = inputs.ScanShape(**{**shape.__dict__, "batch": args.batch or shape.batch,
+                                    "seqlen": args.seqlen or shape.seqlen})
     cfg_name = inputs.CONFIG_NAMES[args.workload]
     world, rank, local = dist_env()
 
@@ -387,7 +389,7 @@ def main():
                    "parallelism": f"weak x{world} (independent sequences per rank)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": (ncu_traffic(cfg_name) if not args.batch else None),
+                     "traffic": (ncu_traffic(cfg_name) if not (args.batch or args.seqlen) else None),
                      "peak_kind": f"{peak_kind} HBM copy bandwidth", "algorithmic_bytes": nbytes,
                      "tensor_tflops": scan_flops(shape) / (ms * 1e-3) / 1e12},
         "gpu_launches": args.steps,

@@ -226,6 +226,27 @@ __device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, uint32_t (&v)[16]
         : "r"(taddr));
 }
 
+// Same lanes, 16 columns per half with the halves 16 columns apart: threads
+// 0-15 get columns [c, c+16), threads 16-31 get [c+16, c+32).
+__device__ __forceinline__ void tmem_ld16x2_16h(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+}
+
+// Same lanes, 8 columns per half with the halves 8 columns apart: threads
+// 0-15 get columns [c, c+8), threads 16-31 get [c+8, c+16) -- one 16-column
+// block of an M = 64 accumulator spread over the whole warp.
+__device__ __forceinline__ void tmem_ld16x2_8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], 8;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+        : "r"(taddr));
+}
+
 // ---------------------------------------------------------------- named barriers
 // Barrier `id` over `count` threads (a multiple of 32) that also ORs a
 // predicate across them: every participant gets the same result, so a
@@ -242,8 +263,10 @@ __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t count, bool pr
         : "memory");
     return out != 0;
 }
+// Plain barrier `id` over `count` threads (not .aligned: the threads of a warp
+// may arrive from divergent code).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
-    asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(count) : "memory");
+    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- descriptors
@@ -257,6 +280,50 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     d |= (uint64_t)2u << 61;  // 128-byte swizzle
     return d;
 }
+// Same with the 64-byte swizzle (atom: 8 rows x 64 bytes; 16-byte chunk c of
+// row r stored at chunk c ^ ((r / 2) % 4), as TMA's CU_TENSOR_MAP_SWIZZLE_64B
+// writes it).  MN-major: rows of 32 bf16 along MN, SBO = 512 (next 8 K rows).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;  // descriptor version for tcgen05
+    d |= (uint64_t)4u << 61;  // 64-byte swizzle
+    return d;
+}
+// Byte offset of bf16 element (row, col) in a 64-byte-swizzled tile of 32
+// columns.
+__host__ __device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t col) {
+    const uint32_t chunk = (col >> 3) ^ ((row >> 1) & 3u);
+    return row * 64u + chunk * 16u + (col & 7u) * 2u;
+}
+
+// The same descriptors split in two 32-bit words: the high word holds only
+// constants (SBO, version, swizzle) and the low word the address and LBO, so
+// that stepping through K is one 32-bit add (no carry: shared-memory
+// addresses are below 2^18).
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo_bytes, uint32_t swizzle) {
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (swizzle << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kSwz128 = 2, kSwz64 = 4;
+// D[tmem] (+)= A * B^T from split descriptors (see above); one thread.
+template <uint32_t A_HI, uint32_t B_HI>
+__device__ __forceinline__ void umma_bf16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+        "mov.b64 ad, {%1, %5};\n\t"
+        "mov.b64 bd, {%2, %6};\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(A_HI), "n"(B_HI)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4)                              // D format: f32

@@ -55,6 +55,11 @@ constexpr int kP = 64;                          // headdim
 constexpr long long kWaitBudget = 4000000000LL; // clock cycles (~2 s) before a wait gives up
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr uint32_t kBarWG0 = 1, kBarWG1 = 2;
+// Largest decay span (log2 units) across one 16-row mask block for which the
+// diagonal block is evaluated in factorised form; beyond it, exactly.
+constexpr float kSpanMax = 96.0f;
+// High word of every 128-byte-swizzled operand descriptor here (SBO = 1024).
+constexpr uint32_t kDescHi = ptx::sdesc_hi(1024, ptx::kSwz128);
 
 __host__ __device__ constexpr int align1k(int x) { return (x + 1023) & ~1023; }
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -65,8 +70,6 @@ struct Cfg {
     static constexpr int N = 64 * NSLAB;         // state size
     static constexpr int K = N / 2;              // rotation pairs
     static constexpr int KG = N / 8;             // 16-byte groups per row (4 pairs each)
-    static constexpr int NSEG = kWG / KG;        // token segments of the angle scan
-    static constexpr int TPS = Q / NSEG;         // tokens per segment
     static constexpr int TB = 16 / R;            // tokens per 16-row mask block
     static constexpr int TILE = kRows * 128;     // one 64-column slab of a 64-row bf16 tile
     // stage (TMA destination): x | B slabs | C slabs | theta
@@ -81,18 +84,21 @@ struct Cfg {
     static constexpr int OFF_SP = OFF_BD + 2 * NSLAB * TILE;  // S' (K-major)
     static constexpr int OFF_G = OFF_SP + TILE;               // G bf16 [N][P] (MN-major)
     static constexpr int OFF_Y = OFF_G + N * 128;             // y staging (TMA store source)
-    static constexpr int OFF_SC = OFF_Y + TILE;               // per-stage scalars
-    static constexpr int SC_CS = 0, SC_W = Q, SC_GAM = 2 * Q, SC_SCB = 3 * Q, SC_SCF = 4 * Q, SC_DEC = 5 * Q;
-    static constexpr int SC_STRIDE = 5 * Q + 4;               // floats per stage
-    static constexpr int OFF_DL = OFF_SC + 2 * SC_STRIDE * 4; // dt[Q+1], lambda[Q+1]
-    static constexpr int OFF_WS = align16(OFF_DL + 2 * (Q + 1) * 4);  // warp sums [4]
-    static constexpr int OFF_PART = OFF_WS + 16;              // angle partials [4 warps][KG][4]
-    static constexpr int OFF_CARRY = align16(OFF_PART + 4 * KG * 16);  // double [K]
-    static constexpr int SMEM_BYTES = OFF_CARRY + K * 8 + 1024;        // + alignment slack
+    static constexpr int OFF_L = OFF_Y + TILE;                // L: [64 rows][64 tokens] 0/1, K-major
+    static constexpr int OFF_SC = OFF_L + TILE;               // per-stage scalars
+    static constexpr int SC_CS = 0, SC_W = Q, SC_GAM = 2 * Q, SC_SCB = 3 * Q, SC_SCF = 4 * Q, SC_SDF = 5 * Q,
+                         SC_DEC = 6 * Q;
+    static constexpr int SC_STRIDE = 6 * Q + 4;               // floats per stage
+    static constexpr int OFF_CARRY = align16(OFF_SC + 2 * SC_STRIDE * 4);  // float [2][K]: angle carry
+    static constexpr int SMEM_BYTES = OFF_CARRY + 2 * K * 4 + 1024;    // + alignment slack
+    // theta tile [Q][K] as the MN-major B operand of Phi = L theta: 64-byte
+    // swizzle for K = 32 pairs, 128-byte swizzle for K = 64
+    static constexpr uint32_t TH_SBO = (K == 32) ? 512 : 1024;
+    static constexpr uint32_t TH_K16 = 2 * TH_SBO;            // bytes per 16 tokens
     // TMEM columns: S / Y_intra double-buffered, dG, Y_inter
     static constexpr uint32_t TM_SY0 = 0, TM_DG = 128, TM_YI = 192, TM_COLS = 256;
-    static_assert(NSEG * TPS == Q, "angle segments must tile the chunk");
-    static_assert(Q % 32 == 0 || Q <= 32, "scalar scan");
+    static_assert(Q <= 64, "scalar lanes hold two tokens each");
+    static_assert(K == 32 || K == 64, "theta tile width");
     static_assert(TB * R == 16, "mask blocks");
 };
 
@@ -110,15 +116,38 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
-    return __bfloat1622float2(v);
+// n consecutive floats from shared memory (n = 8, 4: 16-byte aligned; n = 2: 8-byte aligned).
+template <int n>
+__device__ __forceinline__ void load_tok(const float* p, float (&out)[n]) {
+    if constexpr (n == 2) {
+        const float2 a = *reinterpret_cast<const float2*>(p);
+        out[0] = a.x; out[1] = a.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < n; q += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(p + q);
+            out[q] = a.x; out[q + 1] = a.y; out[q + 2] = a.z; out[q + 3] = a.w;
+        }
+    }
 }
-// sin / cos of x: one reduction to [-pi, pi] by a multiple of 2 pi, then the
-// hardware sin / cos (absolute error ~1e-6 on that range).
-__device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
+
+// The two bf16 of a packed word as floats (bf16 is the top half of an fp32).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// x - n 2 pi with n = rint(x / 2 pi), in [-pi, pi]: Cody and Waite's
+// two-constant reduction (2 pi = kC1 + kC2 with kC1 = 201/32 exact in 8 bits,
+// so n kC1 is exact for |n| < 2^16 and the error is about |n| ulp(kC2)).
+constexpr float kC1 = 6.28125f;
+constexpr float kC2 = 1.9353071795864769e-3f;
+__device__ __forceinline__ float reduce_2pi(float x) {
     const float n = rintf(x * (1.0f / kTwoPi));
-    __sincosf(fmaf(-n, kTwoPi, x), s, c);
+    return fmaf(-n, kC2, fmaf(-n, kC1, x));
+}
+// sin / cos of x: the reduction above, then the hardware sin / cos (absolute
+// error ~1e-6 on [-pi, pi]).
+__device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
+    __sincosf(reduce_2pi(x), s, c);
 }
 // Byte offset of the 16-byte group g of row `row` in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int row, int g) {
@@ -131,10 +160,10 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                       const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_th,
                       const __grid_constant__ CUtensorMap map_y, const Params prm) {
     using CF = Cfg<NSLAB, R, ROT>;
-    constexpr int Q = CF::Q, N = CF::N, K = CF::K, KG = CF::KG, TPS = CF::TPS, TILE = CF::TILE;
+    constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_full[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_fin[2];
+    __shared__ uint64_t bar_full[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_phi, bar_fin[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
 
@@ -151,11 +180,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     const float A_l2 = __ldg(prm.A + h) * m3::kLog2e;
 
     float* scal0 = reinterpret_cast<float*>(smem + CF::OFF_SC);
-    float* s_d = reinterpret_cast<float*>(smem + CF::OFF_DL);
-    float* s_l = s_d + (Q + 1);
-    float* s_ws = reinterpret_cast<float*>(smem + CF::OFF_WS);
-    float* s_part = reinterpret_cast<float*>(smem + CF::OFF_PART);
-    double* s_carry = reinterpret_cast<double*>(smem + CF::OFF_CARRY);
+    float* s_carry = reinterpret_cast<float*>(smem + CF::OFF_CARRY);
     uint8_t* t_sp = smem + CF::OFF_SP;
     uint8_t* t_g = smem + CF::OFF_G;
     uint8_t* t_y = smem + CF::OFF_Y;
@@ -170,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         ptx::mbar_init(&bar_dgfree, 1);
         ptx::mbar_init(&bar_yi, 1);
         ptx::mbar_init(&bar_y, 1);
+        ptx::mbar_init(&bar_phi, 1);
         ptx::fence_mbar_init();
         abort_s = 0;
     }
@@ -177,7 +203,21 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         ptx::tmem_alloc(&tmem_base_s, CF::TM_COLS);
         ptx::tmem_relinquish();
     }
-    if (tid < K) s_carry[tid] = 0.0;
+    if (tid < 2 * K) s_carry[tid] = 0.0f;
+    // L[i][t] = 1 for t <= token(i) = i / R (and t < Q), else 0: 64 x 64 bf16, 128-byte swizzle
+    for (int e = tid; e < kRows * 8; e += kThreads) {
+        const int i = e >> 3, g = e & 7;
+        uint32_t wv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int t0 = g * 8 + 2 * m;
+            const uint32_t lo = (t0 <= i / R && t0 < Q) ? 0x3F80u : 0u;        // bf16 1.0
+            const uint32_t hi = (t0 + 1 <= i / R && t0 + 1 < Q) ? 0x3F80u : 0u;
+            wv[m] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(smem + CF::OFF_L + swz(i, g)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -209,201 +249,243 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 
     if (tid < kWG) {
         // ======================= warpgroup 0: prologue + S / dG issue =======================
-        const int kg = tid % KG, seg = tid / KG;
-        auto load_scalars = [&](int c, float& dv, float& lv, float& dn, float& ln) {
-            const int64_t t = (int64_t)c * Q + tid;
-            dv = 0.0f; lv = 1.0f; dn = 0.0f; ln = 1.0f;
-            if (tid < Q && t < T) {
-                const int64_t idx = ((int64_t)b * T + t) * prm.H + h;
-                dv = __ldg(prm.dt + idx);
-                if (prm.lam) lv = __ldg(prm.lam + idx);
+        // Thread 0 turns the chunk's theta tile into the cumulative angles of
+        // every tile row with one MMA, Phi_rows = L theta (L[i][t] = 1 for
+        // t <= token(i)), into the S/Y TMEM buffer of the stage.  Thread
+        // (warp w, lane l) then owns tile row 16 w + l % 16 and the rotation
+        // pairs [PH (l / 16), PH (l / 16) + PH): it reads those angles with the
+        // 16x32bx2 TMEM shape, rotates its half of the B and C rows in shared
+        // memory (bank-conflict free under the 128-byte swizzle) and writes its
+        // half of the scaled copy B~'.  Every warp computes the chunk scalars
+        // itself (lane l holds tokens l and l + 32).
+        constexpr int PH = K / 2;               // pairs per thread
+        constexpr int GPT = PH / 4;             // 16-byte groups per thread
+        const int row = warp * 16 + (lane & 15);
+        const int hf = lane >> 4;
+        const int tok = row / R;
+        float* carry_buf = reinterpret_cast<float*>(smem + CF::OFF_CARRY);   // [2][K]
+        // dt / lambda of tokens c0 + lane, c0 + 32 + lane and c0 + Q, one chunk ahead
+        auto load_scalars = [&](int c, float (&dv)[2], float (&lv)[2], float& dn, float& ln) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int tt = u * 32 + lane;
+                const int64_t t = (int64_t)c * Q + tt;
+                dv[u] = 0.0f; lv[u] = 1.0f;
+                if (tt < Q && t < T) {
+                    const int64_t idx = ((int64_t)b * T + t) * prm.H + h;
+                    dv[u] = __ldg(prm.dt + idx);
+                    if (prm.lam) lv[u] = __ldg(prm.lam + idx);
+                }
             }
             const int64_t tn = (int64_t)(c + 1) * Q;
-            if (tid == 0 && tn < T) {
+            dn = 0.0f; ln = 1.0f;
+            if (tn < T) {
                 const int64_t idx = ((int64_t)b * T + tn) * prm.H + h;
                 dn = __ldg(prm.dt + idx);
                 if (prm.lam) ln = __ldg(prm.lam + idx);
             }
         };
-        float d_cur, l_cur, dn_cur, ln_cur;
+        float d_cur[2], l_cur[2], dn_cur, ln_cur;
         load_scalars(0, d_cur, l_cur, dn_cur, ln_cur);
 
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             uint8_t* st = smem + s * CF::ST_BYTES;
             float* sc = scal0 + s * CF::SC_STRIDE;
-            float d_nx = 0.0f, l_nx = 1.0f, dn_nx = 0.0f, ln_nx = 1.0f;
-            if (c + 1 < nch) load_scalars(c + 1, d_nx, l_nx, dn_nx, ln_nx);
-
-            // (1) dt / lambda staging, warp scan of dt A (log2 units)
-            if (tid < Q) { s_d[tid] = d_cur; s_l[tid] = l_cur; }
-            if (tid == 0) { s_d[Q] = dn_cur; s_l[Q] = ln_cur; }
-            float a = (tid < Q) ? d_cur * A_l2 : 0.0f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, a, o);
-                if (lane >= o) a += v;
-            }
-            if (lane == 31) s_ws[warp] = a;
-            // this chunk's tiles
-            bool fail = !ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
-            // angle partial sums of this thread's tokens for its 4 pairs
-            float ph[4] = {0.0f, 0.0f, 0.0f, 0.0f}, own[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const __nv_bfloat16* s_th = reinterpret_cast<const __nv_bfloat16*>(st + CF::ST_TH);
-            if (ROT) {   // unconditional: the shuffles below need the whole warp
-#pragma unroll
-                for (int i = 0; i < TPS; ++i) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(s_th + (seg * TPS + i) * K + kg * 4);
-                    const float2 t01 = unpack_bf16(raw.x), t23 = unpack_bf16(raw.y);
-                    own[0] += t01.x; own[1] += t01.y; own[2] += t23.x; own[3] += t23.y;
-                }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) ph[m] = own[m];
-                // inclusive scan over the segments of this warp with the same kg
-#pragma unroll
-                for (int o = KG; o < 32; o <<= 1) {
-                    float v[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) v[m] = __shfl_up_sync(0xffffffffu, ph[m], o);
-                    if (lane >= o) {
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) ph[m] += v[m];
-                    }
-                }
-                if (lane >= 32 - KG) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) s_part[(warp * KG + kg) * 4 + m] = ph[m];
-                }
-            }
-            if (fail) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
-            if (ptx::bar_sync_or(kBarWG0, kWG, fail || abort_s)) { aborted = true; break; }
-
-            // (2) cs, gamma, w; angle at the start of this thread's segment
-            float cs_t = 0.0f;
-            if (tid < Q) {
-                float off = 0.0f;
-                for (int w = 0; w < warp; ++w) off += s_ws[w];
-                cs_t = a + off;
-                const float d = s_d[tid], l = s_l[tid], dn = s_d[tid + 1], ln = s_l[tid + 1];
-                sc[CF::SC_CS + tid] = cs_t;
-                sc[CF::SC_GAM + tid] = l * d;
-                sc[CF::SC_W + tid] = l * d + (1.0f - ln) * dn;
-            }
-            float phi[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (ROT) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    // exclusive prefix: carry + earlier warps + earlier segments of this warp
-                    float run = (float)s_carry[kg * 4 + m];
-                    for (int w = 0; w < warp; ++w) run += s_part[(w * KG + kg) * 4 + m];
-                    phi[m] = run + (ph[m] - own[m]);
-                }
-            }
-            ptx::bar_sync(kBarWG0, kWG);
-
-            // (3) per-token scales: B~' rows, factorised mask columns, chunk decay
-            if (tid < Q) {
-                const float cs_end = sc[CF::SC_CS + Q - 1];
-                const int ref = (tid / CF::TB) * CF::TB + CF::TB - 1;
-                const float w = sc[CF::SC_W + tid];
-                sc[CF::SC_SCB + tid] = exp2f(cs_end - cs_t) * w;
-                sc[CF::SC_SCF + tid] = exp2f(sc[CF::SC_CS + ref] - cs_t) * w;
-                if (tid == 0) sc[CF::SC_DEC] = exp2f(cs_end);
-            }
-            ptx::bar_sync(kBarWG0, kWG);
-
-            // (4) rotate B, C in place (B~, C~) and write B~' = scb * B~
-            {
-                uint8_t* sb = st + CF::ST_B;
-                uint8_t* scc = st + CF::ST_C;
-                uint8_t* bd = smem + CF::OFF_BD + s * NSLAB * TILE;
-#pragma unroll
-                for (int i = 0; i < TPS; ++i) {
-                    const int t = seg * TPS + i;
-                    float cn[4], sn[4];
-                    if (ROT) {
-                        const uint2 raw = *reinterpret_cast<const uint2*>(s_th + t * K + kg * 4);
-                        const float2 t01 = unpack_bf16(raw.x), t23 = unpack_bf16(raw.y);
-                        phi[0] += t01.x; phi[1] += t01.y; phi[2] += t23.x; phi[3] += t23.y;
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) sincos_reduced(phi[m], &sn[m], &cn[m]);
-                    }
-                    const float scb = sc[CF::SC_SCB + t];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int row = t * R + r;
-                        const uint32_t off = swz(row, kg);
-                        uint4 vb = *reinterpret_cast<const uint4*>(sb + off);
-                        uint4 ob;
-                        uint32_t* pb = reinterpret_cast<uint32_t*>(&vb);
-                        uint32_t* qb = reinterpret_cast<uint32_t*>(&ob);
-                        if (ROT) {
-                            uint4 vc = *reinterpret_cast<const uint4*>(scc + off);
-                            uint32_t* pc = reinterpret_cast<uint32_t*>(&vc);
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
-                                const float2 bb = unpack_bf16(pb[m]), cv = unpack_bf16(pc[m]);
-                                const float b0 = bb.x * cn[m] + bb.y * sn[m], b1 = bb.y * cn[m] - bb.x * sn[m];
-                                const float c0 = cv.x * cn[m] + cv.y * sn[m], c1 = cv.y * cn[m] - cv.x * sn[m];
-                                pb[m] = pack_bf16(b0, b1);
-                                pc[m] = pack_bf16(c0, c1);
-                            }
-                            *reinterpret_cast<uint4*>(sb + off) = vb;
-                            *reinterpret_cast<uint4*>(scc + off) = vc;
-                        }
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float2 bb = unpack_bf16(pb[m]);
-                            qb[m] = pack_bf16(bb.x * scb, bb.y * scb);
-                        }
-                        *reinterpret_cast<uint4*>(bd + off) = ob;
-                    }
-                }
-                // angle carry at the chunk's last token, reduced mod 2 pi in fp64
-                if (ROT && seg == CF::NSEG - 1) {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        double v = (double)phi[m];
-                        v -= 6.283185307179586 * rint(v * (1.0 / 6.283185307179586));
-                        s_carry[kg * 4 + m] = v;
-                    }
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            if (ptx::bar_sync_or(kBarWG0, kWG, abort_s)) { aborted = true; break; }
-
-            // (5) thread 0: S = C~ B~^T -> TMEM S/Y[s];  dG = B~'^T X -> TMEM dG
-            if (tid == 0) {
-                bool ok = true;
-                if (c >= 1) ok = ptx::mbar_wait(&bar_dgfree, (c - 1) & 1, kWaitBudget);
+            const uint32_t tm_sy = tmem + CF::TM_SY0 + 64u * s;
+            // (0) thread 0: Phi_rows = L theta -> TMEM S/Y[s] once the tiles are in
+            //     and the buffer is free (chunk c-2's output has been read)
+            if (ROT && tid == 0) {
+                bool ok = ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
                 if (ok && c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
                 if (!ok) {
                     m3::set_status(m3::kStatusWaitTimeout);
                     abort_s = 1;
                 } else {
                     ptx::tc_fence_after();
-                    const uint32_t a_c = ptx::smem_u32(st + CF::ST_C), a_b = ptx::smem_u32(st + CF::ST_B);
-                    const uint32_t a_x = ptx::smem_u32(st + CF::ST_X);
-                    const uint32_t a_bd = ptx::smem_u32(smem + CF::OFF_BD + s * NSLAB * TILE);
+                    const uint32_t l_lo = ptx::sdesc_lo(ptx::smem_u32(smem + CF::OFF_L), 16);
+                    const uint32_t th_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_TH), K * 2);
+                    constexpr uint32_t id_phi = ptx::idesc_bf16(kRows, K, false, true);
+                    constexpr uint32_t th_hi = ptx::sdesc_hi(CF::TH_SBO, K == 32 ? ptx::kSwz64 : ptx::kSwz128);
+#pragma unroll
+                    for (int k16 = 0; k16 < Q / 16; ++k16)
+                        ptx::umma_bf16_lo<kDescHi, th_hi>(tm_sy, l_lo + k16 * 2, th_lo + k16 * (CF::TH_K16 >> 4), id_phi,
+                                                           k16 > 0);
+                    ptx::umma_commit(&bar_phi);
+                }
+            }
+            float d_nx[2] = {0.0f, 0.0f}, l_nx[2] = {1.0f, 1.0f}, dn_nx = 0.0f, ln_nx = 1.0f;
+            if (c + 1 < nch) load_scalars(c + 1, d_nx, l_nx, dn_nx, ln_nx);
+
+            // (1) warp 0: chunk scalars for tokens lane (u = 0) and 32 + lane (u = 1):
+            //     cs (log2 units), gamma, w, B~' row scale, mask column weights
+            if (warp == 0) {
+                float dnext[2], lnext[2];
+                {
+                    const float d0s = __shfl_down_sync(0xffffffffu, d_cur[0], 1);
+                    const float l0s = __shfl_down_sync(0xffffffffu, l_cur[0], 1);
+                    const float d1s = __shfl_down_sync(0xffffffffu, d_cur[1], 1);
+                    const float l1s = __shfl_down_sync(0xffffffffu, l_cur[1], 1);
+                    const float d1f = __shfl_sync(0xffffffffu, d_cur[1], 0);
+                    const float l1f = __shfl_sync(0xffffffffu, l_cur[1], 0);
+                    if (lane + 1 < Q && lane < 31) { dnext[0] = d0s; lnext[0] = l0s; }
+                    else if (lane + 1 == Q) { dnext[0] = dn_cur; lnext[0] = ln_cur; }
+                    else if (lane == 31 && Q > 32) { dnext[0] = d1f; lnext[0] = l1f; }
+                    else { dnext[0] = 0.0f; lnext[0] = 1.0f; }       // padding rows of a short chunk
+                    dnext[1] = (lane < 31) ? d1s : dn_cur;
+                    lnext[1] = (lane < 31) ? l1s : ln_cur;
+                }
+                float cs[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float a = d_cur[u] * A_l2;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float v = __shfl_up_sync(0xffffffffu, a, o);
+                        if (lane >= o) a += v;
+                    }
+                    cs[u] = a;
+                }
+                cs[1] += __shfl_sync(0xffffffffu, cs[0], 31);
+                const float cs_end = (Q == 64) ? __shfl_sync(0xffffffffu, cs[1], 31) : __shfl_sync(0xffffffffu, cs[0], Q - 1);
+                const int ref = (lane / CF::TB) * CF::TB + CF::TB - 1;   // last token of the mask block
+                const int first = (lane / CF::TB) * CF::TB;                // its first token
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float cs_ref = __shfl_sync(0xffffffffu, cs[u], ref);
+                    const float cs_first = __shfl_sync(0xffffffffu, cs[u], first);
+                    const float gam = l_cur[u] * d_cur[u];
+                    const float w = gam + (1.0f - lnext[u]) * dnext[u];
+                    const int t = u * 32 + lane;
+                    if (t < Q) {
+                        sc[CF::SC_CS + t] = cs[u];
+                        sc[CF::SC_GAM + t] = gam;
+                        sc[CF::SC_W + t] = w;
+                        sc[CF::SC_SCB + t] = m3::ex2_approx(cs_end - cs[u]) * w;
+                        sc[CF::SC_SCF + t] = m3::ex2_approx(cs_ref - cs[u]) * w;
+                        // >= w; bounded by 2^kSpanMax w wherever the consumer uses it
+                        sc[CF::SC_SDF + t] = m3::ex2_approx(fminf(cs_first - cs[u], kSpanMax)) * w;
+                    }
+                }
+                if (lane == 0) sc[CF::SC_DEC] = m3::ex2_approx(cs_end);
+            }
+
+            // (2) this chunk's tiles; the angles of this thread's row and pairs
+            bool fail = !ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
+            float cn[PH], sn[PH];
+            if (ROT) {
+                if (!fail) fail = !ptx::mbar_wait(&bar_phi, c & 1, kWaitBudget);
+                __syncwarp();   // tcgen05.ld below is warp-aligned
+                ptx::tc_fence_after();
+                const float* cin = carry_buf + s * K + hf * PH;
+                float* cout = carry_buf + (s ^ 1) * K + hf * PH;
+                const uint32_t taddr = tm_sy + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+                for (int q = 0; q < PH; q += 16) {
+                    uint32_t v[16];
+                    if constexpr (PH == 16) ptx::tmem_ld16x2_16h(taddr, v);       // pairs [16 hf, 16 hf + 16)
+                    else ptx::tmem_ld16x2_16(taddr + q, v);                          // pairs 32 hf + q + [0, 16)
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const float4 cv = *reinterpret_cast<const float4*>(cin + q + e);
+                        const float car[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float phi = car[m] + __uint_as_float(v[e + m]);
+                            sincos_reduced(phi, &sn[q + e + m], &cn[q + e + m]);
+                            // the chunk's last row carries its angles to the next chunk
+                            if (row == kRows - 1) cout[q + e + m] = reduce_2pi(phi);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+            }
+
+            // (3) rotate this thread's half rows of B, C in place (B~, C~); after
+            //     warp 0's scalars are in, write B~' = scale * B~
+            {
+                uint8_t* sb = st + CF::ST_B;
+                uint8_t* scc = st + CF::ST_C;
+                uint8_t* bd = smem + CF::OFF_BD + s * NSLAB * TILE;
+                uint4 vb[GPT];
+#pragma unroll
+                for (int g = 0; g < GPT; ++g) vb[g] = *reinterpret_cast<const uint4*>(sb + swz(row, hf * GPT + g));
+                if (ROT) {
+                    uint4 vc[GPT];
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        uint32_t* pb = reinterpret_cast<uint32_t*>(&vb[g]);
+                        uint32_t* pc = reinterpret_cast<uint32_t*>(&vc[g]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos), for the
+                            // B pair and the C pair at once: u = (a_B, a_C), v = (b_B, b_C)
+                            const float2 u = make_float2(bf_lo(pb[m]), bf_lo(pc[m]));
+                            const float2 v = make_float2(bf_hi(pb[m]), bf_hi(pc[m]));
+                            const float co = cn[g * 4 + m], si = sn[g * 4 + m];
+                            const float2 c2 = make_float2(co, co), s2 = make_float2(si, si), ns2 = make_float2(-si, -si);
+                            const float2 u2 = __ffma2_rn(u, c2, __fmul2_rn(v, s2));
+                            const float2 v2 = __ffma2_rn(v, c2, __fmul2_rn(u, ns2));
+                            pb[m] = pack_bf16(u2.x, v2.x);
+                            pc[m] = pack_bf16(u2.y, v2.y);
+                        }
+                        const uint32_t off = swz(row, hf * GPT + g);
+                        *reinterpret_cast<uint4*>(sb + off) = vb[g];
+                        *reinterpret_cast<uint4*>(scc + off) = vc[g];
+                    }
+                }
+                ptx::bar_sync(kBarWG0, kWG);   // warp 0's scalars are in shared memory
+                const float rs = sc[CF::SC_SCB + tok];
+#pragma unroll
+                for (int g = 0; g < GPT; ++g) {
+                    // B~' = scale * B~ (from the rounded B~, as the MMA sees it)
+                    const uint32_t* pb = reinterpret_cast<const uint32_t*>(&vb[g]);
+                    *reinterpret_cast<uint4*>(bd + swz(row, hf * GPT + g)) =
+                        make_uint4(pack_bf16(bf_lo(pb[0]) * rs, bf_hi(pb[0]) * rs),
+                                   pack_bf16(bf_lo(pb[1]) * rs, bf_hi(pb[1]) * rs),
+                                   pack_bf16(bf_lo(pb[2]) * rs, bf_hi(pb[2]) * rs),
+                                   pack_bf16(bf_lo(pb[3]) * rs, bf_hi(pb[3]) * rs));
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            if (fail) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
+            if (ptx::bar_sync_or(kBarWG0, kWG, fail || abort_s)) { aborted = true; break; }
+
+            // (5) thread 0: S = C~ B~^T -> TMEM S/Y[s];  dG = B~'^T X -> TMEM dG
+            if (tid == 0) {
+                bool ok = true;
+                if (c >= 1) ok = ptx::mbar_wait(&bar_dgfree, (c - 1) & 1, kWaitBudget);
+                if (!ROT && ok && c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
+                if (!ok) {
+                    m3::set_status(m3::kStatusWaitTimeout);
+                    abort_s = 1;
+                } else {
+                    ptx::tc_fence_after();
+                    const uint32_t c_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_C), 16);
+                    const uint32_t b_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_B), 16);
+                    const uint32_t x_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_X), TILE);
+                    const uint32_t bd_lo = ptx::sdesc_lo(ptx::smem_u32(smem + CF::OFF_BD + s * NSLAB * TILE), TILE);
                     constexpr uint32_t id_s = ptx::idesc_bf16(kRows, kRows, false, false);
                     constexpr uint32_t id_g = ptx::idesc_bf16(N, kP, true, true);
                     const uint32_t tm_s = tmem + CF::TM_SY0 + 64u * s;
 #pragma unroll
                     for (int k16 = 0; k16 < N / 16; ++k16) {   // K = state (K-major slabs)
-                        const uint32_t ko = (k16 >> 2) * TILE + (k16 & 3) * 32;
-                        ptx::umma_bf16(tm_s, ptx::sdesc_sw128(a_c + ko, 16, 1024), ptx::sdesc_sw128(a_b + ko, 16, 1024),
-                                       id_s, k16 > 0);
+                        const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
+                        ptx::umma_bf16_lo<kDescHi, kDescHi>(tm_s, c_lo + ko, b_lo + ko, id_s, k16 > 0);
                     }
 #pragma unroll
-                    for (int k16 = 0; k16 < kRows / 16; ++k16) {   // K = rows (MN-major operands)
-                        ptx::umma_bf16(tmem + CF::TM_DG, ptx::sdesc_sw128(a_bd + k16 * 2048, TILE, 1024),
-                                       ptx::sdesc_sw128(a_x + k16 * 2048, TILE, 1024), id_g, k16 > 0);
-                    }
+                    for (int k16 = 0; k16 < kRows / 16; ++k16)   // K = rows (MN-major operands)
+                        ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + CF::TM_DG, bd_lo + k16 * 128, x_lo + k16 * 128, id_g,
+                                                             k16 > 0);
                     ptx::umma_commit(&bar_sd[s]);
                 }
             }
-            d_cur = d_nx; l_cur = l_nx; dn_cur = dn_nx; ln_cur = ln_nx;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) { d_cur[u] = d_nx[u]; l_cur[u] = l_nx[u]; }
+            dn_cur = dn_nx; ln_cur = ln_nx;
         }
     } else {
         // ======================= warpgroup 1: mask, state, output =======================
@@ -428,63 +510,82 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             const uint32_t tm_sy = tmem + lane_base + CF::TM_SY0 + 64u * s;
             // (1) S_c and dG_c are in TMEM
             bool fail = !ptx::mbar_wait(&bar_sd[s], (c >> 1) & 1, kWaitBudget);
+            __syncwarp();   // tcgen05.ld / wait::ld below are warp-aligned
             ptx::tc_fence_after();
+            // S_c, block J (columns 16 J + [0, 16)) in v[8 J, 8 J + 8): this thread
+            // holds columns 16 J + 8 hc + [0, 8) (waited for in the mask below)
+            uint32_t v[32];
+#pragma unroll
+            for (int J = 0; J < 4; ++J) ptx::tmem_ld16x2_8(tm_sy + 16 * J, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * J]));
             if (leader && !fail && c > 0) {
                 // Y_inter = C~ G_{c-1} (G: bf16 [N][P] rows, MN-major)
-                const uint32_t a_c = ptx::smem_u32(st + CF::ST_C), a_g = ptx::smem_u32(t_g);
+                const uint32_t c_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_C), 16);
+                const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(t_g), N * 128);
                 constexpr uint32_t id_y = ptx::idesc_bf16(kRows, kP, false, true);
 #pragma unroll
                 for (int k16 = 0; k16 < N / 16; ++k16) {
-                    const uint32_t ko = (k16 >> 2) * TILE + (k16 & 3) * 32;
-                    ptx::umma_bf16(tmem + CF::TM_YI, ptx::sdesc_sw128(a_c + ko, 16, 1024),
-                                   ptx::sdesc_sw128(a_g + k16 * 2048, N * 128, 1024), id_y, k16 > 0);
+                    const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + CF::TM_YI, c_lo + ko, g_lo + k16 * 128, id_y, k16 > 0);
                 }
                 ptx::umma_commit(&bar_yi);
             }
-            // (2) mask: S' = S o M for this thread's row and 32 columns
+            // (2) mask: S' = S o M for this thread's row, 8 columns in each of the
+            //     four 16-row blocks; the block kind (below / diagonal / above)
+            //     is the same for the whole warp
             const float cs_i = sc[CF::SC_CS + ti];
             {
-                uint32_t v[32];
-                ptx::tmem_ld16x2_32(tm_sy, v);
-                ptx::tmem_ld_wait();
+                constexpr int TB = CF::TB;
+                constexpr int TPC = 8 / R;                         // tokens under 8 columns
                 const float gam_i = sc[CF::SC_GAM + ti];
-                uint32_t o[16];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int J = hc * 2 + half;                   // 16-row block of these 16 columns
+                for (int J = 0; J < 4; ++J) {
+                    const int t0 = (16 * J + 8 * hc) / R;         // first token of these columns
+                    float mk[TPC];
                     if (J < w1) {
-                        const float u = exp2f(cs_i - sc[CF::SC_CS + J * CF::TB + CF::TB - 1]);
+                        // strictly below the diagonal block: exp(cs_i - cs_r) * [exp(cs_r - cs_j) w_j]
+                        const float u = m3::ex2_approx(cs_i - sc[CF::SC_CS + J * TB + TB - 1]);
+                        load_tok<TPC>(sc + CF::SC_SCF + t0, mk);
 #pragma unroll
-                        for (int jj = 0; jj < 16; jj += 2) {
-                            const int j = J * 16 + jj;
-                            const float m0 = u * sc[CF::SC_SCF + j / R], m1 = u * sc[CF::SC_SCF + (j + 1) / R];
-                            o[half * 8 + jj / 2] = pack_bf16(__uint_as_float(v[half * 16 + jj]) * m0,
-                                                             __uint_as_float(v[half * 16 + jj + 1]) * m1);
-                        }
+                        for (int e = 0; e < TPC; ++e) mk[e] *= u;
                     } else if (J == w1) {
+                        // diagonal block: exp(cs_i - cs_f) * [exp(cs_f - cs_j) w_j] around the
+                        // block's first token f while its decay span stays below 2^kSpanMax
+                        // (both factors finite), else one exp per token
+                        const float cs_f = sc[CF::SC_CS + J * TB];
+                        if (cs_f - sc[CF::SC_CS + J * TB + TB - 1] <= kSpanMax) {
+                            const float e_i = m3::ex2_approx(cs_i - cs_f);
+                            load_tok<TPC>(sc + CF::SC_SDF + t0, mk);
 #pragma unroll
-                        for (int jj = 0; jj < 16; jj += 2) {
-                            float mm[2];
+                            for (int e = 0; e < TPC; ++e) mk[e] *= e_i;
+                        } else {
 #pragma unroll
-                            for (int u2 = 0; u2 < 2; ++u2) {
-                                const int tj = (J * 16 + jj + u2) / R;
-                                mm[u2] = (tj < ti) ? exp2f(cs_i - sc[CF::SC_CS + tj]) * sc[CF::SC_W + tj]
-                                                   : (tj == ti ? gam_i : 0.0f);
-                            }
-                            o[half * 8 + jj / 2] = pack_bf16(__uint_as_float(v[half * 16 + jj]) * mm[0],
-                                                             __uint_as_float(v[half * 16 + jj + 1]) * mm[1]);
+                            for (int e = 0; e < TPC; ++e)
+                                mk[e] = m3::ex2_approx(cs_i - sc[CF::SC_CS + t0 + e]) * sc[CF::SC_W + t0 + e];
                         }
+#pragma unroll
+                        for (int e = 0; e < TPC; ++e)
+                            mk[e] = (t0 + e < ti) ? mk[e] : (t0 + e == ti ? gam_i : 0.0f);
                     } else {
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) o[half * 8 + jj] = 0u;
+                        for (int e = 0; e < TPC; ++e) mk[e] = 0.0f;
                     }
-                }
+                    if (J == 0) {
+                        __syncwarp();
+                        ptx::tmem_ld_wait();
+                    }
+                    uint32_t o[4];
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    *reinterpret_cast<uint4*>(t_sp + swz(i_row, hc * 4 + g)) =
-                        make_uint4(o[g * 4 + 0], o[g * 4 + 1], o[g * 4 + 2], o[g * 4 + 3]);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 sv = __fmul2_rn(
+                            make_float2(__uint_as_float(v[8 * J + e]), __uint_as_float(v[8 * J + e + 1])),
+                            make_float2(mk[e / R], mk[(e + 1) / R]));
+                        o[e / 2] = pack_bf16(sv.x, sv.y);
+                    }
+                    *reinterpret_cast<uint4*>(t_sp + swz(i_row, 2 * J + hc)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
             }
             // (3) G_c = exp(cs_end) G_{c-1} + dG_c (fp32)
+            __syncwarp();
             {
                 const float dec = sc[CF::SC_DEC];
                 if constexpr (N == 64) {
@@ -492,7 +593,11 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     ptx::tmem_ld16x2_32(tmem + lane_base + CF::TM_DG, v);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int p = 0; p < 32; ++p) G[p] = fmaf(dec, G[p], __uint_as_float(v[p]));
+                    for (int p = 0; p < 32; p += 2) {
+                        const float2 g2 = __ffma2_rn(make_float2(dec, dec), make_float2(G[p], G[p + 1]),
+                                                     make_float2(__uint_as_float(v[p]), __uint_as_float(v[p + 1])));
+                        G[p] = g2.x; G[p + 1] = g2.y;
+                    }
                 } else {
 #pragma unroll
                     for (int c32 = 0; c32 < 2; ++c32) {
@@ -500,8 +605,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                         ptx::tmem_ld32(tmem + lane_base + CF::TM_DG + c32 * 32, v);
                         ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int p = 0; p < 32; ++p)
-                            G[c32 * 32 + p] = fmaf(dec, G[c32 * 32 + p], __uint_as_float(v[p]));
+                        for (int p = 0; p < 32; p += 2) {
+                            const float2 g2 = __ffma2_rn(make_float2(dec, dec),
+                                                         make_float2(G[c32 * 32 + p], G[c32 * 32 + p + 1]),
+                                                         make_float2(__uint_as_float(v[p]), __uint_as_float(v[p + 1])));
+                            G[c32 * 32 + p] = g2.x; G[c32 * 32 + p + 1] = g2.y;
+                        }
                     }
                 }
             }
@@ -514,12 +623,13 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 ptx::tc_fence_after();
                 ptx::mbar_arrive(&bar_dgfree);
                 // Y_intra = S' X -> TMEM S/Y[s] (S has been read by every thread)
-                const uint32_t a_sp = ptx::smem_u32(t_sp), a_x = ptx::smem_u32(st + CF::ST_X);
+                const uint32_t sp_lo = ptx::sdesc_lo(ptx::smem_u32(t_sp), 16);
+                const uint32_t x_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_X), TILE);
                 constexpr uint32_t id_y = ptx::idesc_bf16(kRows, kP, false, true);
 #pragma unroll
                 for (int k16 = 0; k16 < kRows / 16; ++k16)
-                    ptx::umma_bf16(tmem + CF::TM_SY0 + 64u * s, ptx::sdesc_sw128(a_sp + k16 * 32, 16, 1024),
-                                   ptx::sdesc_sw128(a_x + k16 * 2048, TILE, 1024), id_y, k16 > 0);
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + CF::TM_SY0 + 64u * s, sp_lo + k16 * 2, x_lo + k16 * 128,
+                                                         id_y, k16 > 0);
                 ptx::umma_commit(&bar_y);
             }
             // (4) G_{c-1} is no longer read: store the bf16 copy of G_c
@@ -540,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }
             // (5) Y_intra done: stage s is free -> TMA of chunk c + 2
             if (!fail) fail = !ptx::mbar_wait(&bar_y, c & 1, kWaitBudget);
+            __syncwarp();
             ptx::tc_fence_after();
             if (leader && !fail && c + 2 < nch) {
                 issue_loads(c + 2);
@@ -547,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }
             // (6) y = Y_intra + exp(cs) Y_inter -> bf16 staging -> TMA store
             {
-                const float e = exp2f(cs_i);
+                const float e = m3::ex2_approx(cs_i);
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t ya[16], yb[16];
@@ -556,8 +667,14 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     ptx::tmem_ld_wait();
                     float y[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        y[j] = (c > 0) ? fmaf(e, __uint_as_float(yb[j]), __uint_as_float(ya[j])) : __uint_as_float(ya[j]);
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 a2 = make_float2(__uint_as_float(ya[j]), __uint_as_float(ya[j + 1]));
+                        float2 r2 = a2;
+                        if (c > 0)
+                            r2 = __ffma2_rn(make_float2(e, e), make_float2(__uint_as_float(yb[j]), __uint_as_float(yb[j + 1])),
+                                            a2);
+                        y[j] = r2.x; y[j + 1] = r2.y;
+                    }
                     // columns 32 hc + 16 q + [0, 16) -> groups 4 hc + 2 q, +1
 #pragma unroll
                     for (int g = 0; g < 2; ++g)
@@ -590,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         const int g_row = (N == 64) ? (w1 * 16 + (lane & 15)) : (w1 * 32 + lane);
         const int col0 = (N == 64) ? (lane >> 4) * 32 : 0;
         float cn = 1.0f, sn = 0.0f;
-        if (ROT) sincosf((float)s_carry[g_row >> 1], &sn, &cn);
+        if (ROT) sincosf(s_carry[(nch & 1) * K + (g_row >> 1)], &sn, &cn);
         const bool even = (g_row & 1) == 0;
         float* fs = prm.final_state + (((int64_t)b * prm.H + h) * N + g_row) * kP + col0;
 #pragma unroll
@@ -670,15 +787,18 @@ inline bool make_map5(CUtensorMap* m, const void* base, const m3_dims& d, int in
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map over theta [b, T, h, K] bf16: box (K, 1, Q, 1), no swizzle.
+// 4-D map over theta [b, T, h, K] bf16: box (K, 1, Q, 1); the tile is the
+// MN-major operand of the angle MMA, so it lands 64-byte swizzled (K = 32
+// pairs, 64-byte rows) or 128-byte swizzled (K = 64).
 inline bool make_map_theta(CUtensorMap* m, const void* base, const m3_dims& d, int Q) {
     const cuuint64_t K = (cuuint64_t)d.dstate / 2;
     cuuint64_t dims[4] = {K, (cuuint64_t)d.heads, (cuuint64_t)d.seqlen, (cuuint64_t)d.batch};
     cuuint64_t strides[3] = {K * 2, (cuuint64_t)d.heads * K * 2, (cuuint64_t)d.seqlen * d.heads * K * 2};
     cuuint32_t box[4] = {(cuuint32_t)K, 1, (cuuint32_t)Q, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle sw = (K == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -19,8 +19,9 @@ constexpr int kThreads = 128;
 
 // A tile of `rows` (M or N index) x K, bf16, K-major: slab s of 64 K holds
 // rows x 128 bytes.  MN-major: block m of 64 rows holds K x 128 bytes.
-__device__ uint32_t tile_offset(bool mn_major, int rows, int K, int r, int k) {
-    if (!mn_major) return (uint32_t)(k / 64) * rows * 128u + ptx::sw128_offset(r, k % 64);
+__device__ uint32_t tile_offset(int mode, int rows, int K, int r, int k) {
+    if (mode == 0) return (uint32_t)(k / 64) * rows * 128u + ptx::sw128_offset(r, k % 64);
+    if (mode == 2) return ptx::sw64_offset(k, r);   // MN-major, 64-byte swizzle, rows = 32
     return (uint32_t)(r / 64) * K * 128u + ptx::sw128_offset(k, r % 64);
 }
 
@@ -64,12 +65,13 @@ __global__ void umma_probe_kernel(int M, int N, int K, int a_mn, int b_mn, int h
 
     if (tid == 0) {
         const uint32_t a0 = ptx::smem_u32(sa), b0 = ptx::smem_u32(sb);
-        const uint32_t idesc = ptx::idesc_bf16(M, N, a_mn != 0, b_mn != 0);
+        const uint32_t idesc = ptx::idesc_bf16(M, N, a_mn != 0, b_mn != 0);   // b_mn 2: MN-major too
         for (int k16 = 0; k16 < K / 16; ++k16) {
             uint64_t ad, bd;
             if (a_mn) ad = ptx::sdesc_sw128(a0 + k16 * 2048u, (uint32_t)K * 128u, 1024u);
             else ad = ptx::sdesc_sw128(a0 + (k16 / 4) * M * 128u + (k16 % 4) * 32u, 16u, 1024u);
-            if (b_mn) bd = ptx::sdesc_sw128(b0 + k16 * 2048u, (uint32_t)K * 128u, 1024u);
+            if (b_mn == 2) bd = ptx::sdesc_sw64(b0 + k16 * 1024u, 64u, 512u);
+            else if (b_mn) bd = ptx::sdesc_sw128(b0 + k16 * 2048u, (uint32_t)K * 128u, 1024u);
             else bd = ptx::sdesc_sw128(b0 + (k16 / 4) * N * 128u + (k16 % 4) * 32u, 16u, 1024u);
             ptx::umma_bf16(tmem, ad, bd, idesc, k16 > 0 ? 1u : 0u);
         }
@@ -82,7 +84,7 @@ __global__ void umma_probe_kernel(int M, int N, int K, int a_mn, int b_mn, int h
     if (ok && !half_split) {
         for (int c = 0; c < N; c += 16) {
             uint32_t v[16];
-            ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+            ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);   // N is a multiple of 16
             ptx::tmem_ld_wait();
             for (int j = 0; j < 16; ++j) D[(size_t)(warp * 32 + lane) * N + c + j] = __uint_as_float(v[j]);
         }
@@ -136,8 +138,9 @@ extern "C" {
 __attribute__((visibility("default"))) int probe_umma(int M, int N, int K, int a_mn, int b_mn, int half_split,
                                                       const void* A, const void* B, float* D,
                                                       unsigned* status) {
-    if (!(M == 64 || M == 128) || !(N == 64 || N == 128 || N == 256) || !(K == 64 || K == 128)) return -1;
+    if (!(M == 64 || M == 128) || !(N == 32 || N == 64 || N == 128 || N == 256) || !(K == 64 || K == 128)) return -1;
     if (half_split && M != 64) return -1;
+    if ((b_mn == 2) != (N == 32)) return -1;   // the 64-byte-swizzled operand is 32 wide
     const size_t smem = (size_t)(M + N) * K * 2 + 1024;
     cudaFuncSetAttribute(umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     umma_probe_kernel<<<1, kThreads, smem>>>(M, N, K, a_mn, b_mn, half_split, (const __nv_bfloat16*)A,

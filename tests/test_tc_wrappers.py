@@ -111,3 +111,16 @@ def test_tmem_ld_16x32bx2(probe, N):
     D, ref = run_umma(probe, 64, N, 64, 0, 1, seed=5, half_split=1)
     err = np.abs(D[:64] - ref).max() / np.abs(ref).max()
     assert err < 1e-5, err
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [64, 128])
+def test_umma_b_mn_major_sw64(probe, M):
+    """A 32-wide MN-major B operand in the 64-byte swizzle (the layout TMA's
+    64-byte swizzle writes for a [K][32] bf16 tile)."""
+    D, ref = run_umma(probe, M, 32, 64, 0, 2, seed=11)
+    if M == 64:
+        lanes = [m64_lane(i) for i in range(64)]
+        D = D[lanes]
+    err = np.abs(D[:M] - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
