@@ -298,6 +298,8 @@ def main():
     ap.add_argument("--ref-units", type=int, default=32, help="sequences in the oracle sample (cpu_baseline)")
     ap.add_argument("--ref-budget-s", type=float, default=150.0, help="wall budget of the reference arm")
     ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--cpu-rows", type=int, default=8, help="batch rows in the oracle's cpu_baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time the cpu_baseline repeats for")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen (profiling captures)")
     ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
@@ -451,11 +453,25 @@ def main():
         result["decode"] = dec
 
     if not args.no_cpu_baseline and rank == 0:
-        sample, nu = oracle_sample(shape, args.workload, args.ref_units)
-        tps, sec, thr = time_cpu_oracle(shape, sample, nu)
-        result["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
-                                  "sample": f"batch row 0, heads 0..{args.ref_units - 1}, full T={T} "
-                                            f"({sec:.1f} s)"}
+        # the oracle on every host core: the workload's first batch rows (all
+        # heads, full T), repeated until about args.cpu_seconds of wall time
+        import oracle
+        full = inputs.make_scan_inputs(shape, args.workload)
+        rows = max(1, min(shape.batch, args.cpu_rows))
+        sample = {k: (None if v is None else (v if k == "A" else v[:rows].contiguous())) for k, v in full.items()}
+        del full
+        nthreads = oracle.max_threads()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.scan(sample["x"], sample["dt"], sample["A"], sample["B"], sample["C"], sample["lam"],
+                        sample["theta"], nthreads=nthreads)
+            reps += 1
+            if time.perf_counter() - t0 >= args.cpu_seconds:
+                break
+        sec = (time.perf_counter() - t0) / reps
+        result["cpu_baseline"] = {"value": rows * T / sec, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                                  "sample": f"batch rows 0..{rows - 1} x all {H} heads x full T={T} of the workload, "
+                                            f"{reps} repetition(s), {sec:.2f} s each"}
 
     if world > 1:
         import torch.distributed as dist

@@ -9,6 +9,7 @@
 #include "m3scan.h"
 #include "common.cuh"
 #include "step_simt.cuh"
+#include "step_fast.cuh"
 #include "scan_ws.cuh"
 
 namespace {
@@ -131,6 +132,36 @@ int dispatch_step(const m3_dims* d, float* state, const void* x_t, const float* 
     return M3_ERR_UNSUPPORTED;
 }
 
+// The decode step for the common shapes (step_fast.cuh); every tensor is
+// 16-byte aligned (checked by the caller).
+template <typename T>
+int launch_step_fast(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A,
+                     const void* B_t, const void* C_t, const float* lam_t, const void* theta_t, const void* prev_B,
+                     const void* prev_x, void* y_t, cudaStream_t s) {
+    m3fast::StepArgs a;
+    a.H = (int)d->heads;
+    a.N = (int)d->dstate;
+    a.P = (int)d->headdim;
+    a.P4 = a.P / 4;
+    const int block = m3fast::threads(d->dstate, d->headdim);
+    const size_t smem = m3fast::smem_bytes(d->dstate, d->headdim, d->rank);
+    const unsigned grid = (unsigned)(d->batch * d->heads);
+#define M3_STEP_FAST(RR, MT)                                                                                  \
+    m3fast::m3_step_fast_kernel<T, RR, MT><<<grid, block, smem, s>>>(a, state, (const T*)x_t, dt_t, A,          \
+                                                                     (const T*)B_t, (const T*)C_t, lam_t,       \
+                                                                     (const T*)theta_t, (const T*)prev_B,       \
+                                                                     (const T*)prev_x, (T*)y_t)
+    const bool small = block <= 128;
+    switch (d->rank) {
+        case 1: if (small) M3_STEP_FAST(1, 128); else M3_STEP_FAST(1, 256); break;
+        case 2: if (small) M3_STEP_FAST(2, 128); else M3_STEP_FAST(2, 256); break;
+        case 4: if (small) M3_STEP_FAST(4, 128); else M3_STEP_FAST(4, 256); break;
+        default: return M3_ERR_UNSUPPORTED;
+    }
+#undef M3_STEP_FAST
+    return launch_status();
+}
+
 int scan_algorithm(const m3_dims* d) {
     if (check_dims(d, true) != M3_OK) return M3_ALGO_NONE;
     if (m3ws::supports(*d)) return M3_ALGO_CHUNKED_TC;
@@ -202,6 +233,20 @@ int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, 
     for (const void* p : f32_ptrs)
         if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
     if (state && !aligned16(state)) return M3_ERR_ALIGN;
+    if (m3fast::supports(d->dstate, d->headdim, d->rank)) {
+        const void* vec_ptrs[] = {state, x_t, B_t, C_t, theta_t, prev_B, prev_x};
+        bool ok16 = true;
+        for (const void* p : vec_ptrs) ok16 = ok16 && (!p || aligned16(p));
+        if (ok16) {
+            if (d->batch == 0) return M3_OK;
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            return d->dtype == M3_F32
+                       ? launch_step_fast<float>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x,
+                                                 y_t, s)
+                       : launch_step_fast<__nv_bfloat16>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B,
+                                                         prev_x, y_t, s);
+        }
+    }
     SimtArgs a;
     int npt, block;
     if (!simt_geometry(d, &a, &npt, &block) || step_smem_bytes(a) > kMaxSmem) return M3_ERR_UNSUPPORTED;
