@@ -287,33 +287,54 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         };
         float d_cur[2], l_cur[2], dn_cur, ln_cur;
         load_scalars(0, d_cur, l_cur, dn_cur, ln_cur);
+        // thread 0 only: the MMAs of step (0) for chunk c (c = nch: the last Y_inter)
+        auto issue_early = [&](int c) {
+            const int s = c & 1;
+            bool ok = true;
+            if (c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
+            if (ok && ROT && c < nch) ok = ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
+            if (!ok) {
+                m3::set_status(m3::kStatusWaitTimeout);
+                abort_s = 1;
+                return;
+            }
+            ptx::tc_fence_after();
+            if (ROT && c < nch) {
+                const uint32_t l_lo = ptx::sdesc_lo(ptx::smem_u32(smem + CF::OFF_L), 16);
+                const uint32_t th_lo = ptx::sdesc_lo(ptx::smem_u32(smem + s * CF::ST_BYTES + CF::ST_TH), K * 2);
+                constexpr uint32_t id_phi = ptx::idesc_bf16(kRows, K, false, true);
+                constexpr uint32_t th_hi = ptx::sdesc_hi(CF::TH_SBO, K == 32 ? ptx::kSwz64 : ptx::kSwz128);
+#pragma unroll
+                for (int k16 = 0; k16 < Q / 16; ++k16)
+                    ptx::umma_bf16_lo<kDescHi, th_hi>(tmem + CF::TM_SY0 + 64u * s, l_lo + k16 * 2,
+                                                       th_lo + k16 * (CF::TH_K16 >> 4), id_phi, k16 > 0);
+                ptx::umma_commit(&bar_phi);
+            }
+            if (c >= 2) {
+                // Y_inter(c-1) = C~_{c-1} G_{c-2} (G: bf16 [N][P] rows, MN-major)
+                const uint32_t c_lo =
+                    ptx::sdesc_lo(ptx::smem_u32(smem + ((c - 1) & 1) * CF::ST_BYTES + CF::ST_C), 16);
+                const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(t_g), N * 128);
+                constexpr uint32_t id_y = ptx::idesc_bf16(kRows, kP, false, true);
+#pragma unroll
+                for (int k16 = 0; k16 < N / 16; ++k16) {
+                    const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + CF::TM_YI, c_lo + ko, g_lo + k16 * 128, id_y, k16 > 0);
+                }
+                ptx::umma_commit(&bar_yi);
+            }
+        };
 
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             uint8_t* st = smem + s * CF::ST_BYTES;
             float* sc = scal0 + s * CF::SC_STRIDE;
             const uint32_t tm_sy = tmem + CF::TM_SY0 + 64u * s;
-            // (0) thread 0: Phi_rows = L theta -> TMEM S/Y[s] once the tiles are in
-            //     and the buffer is free (chunk c-2's output has been read)
-            if (ROT && tid == 0) {
-                bool ok = ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
-                if (ok && c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
-                if (!ok) {
-                    m3::set_status(m3::kStatusWaitTimeout);
-                    abort_s = 1;
-                } else {
-                    ptx::tc_fence_after();
-                    const uint32_t l_lo = ptx::sdesc_lo(ptx::smem_u32(smem + CF::OFF_L), 16);
-                    const uint32_t th_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_TH), K * 2);
-                    constexpr uint32_t id_phi = ptx::idesc_bf16(kRows, K, false, true);
-                    constexpr uint32_t th_hi = ptx::sdesc_hi(CF::TH_SBO, K == 32 ? ptx::kSwz64 : ptx::kSwz128);
-#pragma unroll
-                    for (int k16 = 0; k16 < Q / 16; ++k16)
-                        ptx::umma_bf16_lo<kDescHi, th_hi>(tm_sy, l_lo + k16 * 2, th_lo + k16 * (CF::TH_K16 >> 4), id_phi,
-                                                           k16 > 0);
-                    ptx::umma_commit(&bar_phi);
-                }
-            }
+            // (0) thread 0, once chunk c-2's output has been read (its S/Y buffer and
+            //     Y_inter free): Phi_rows = L theta -> TMEM S/Y[s] when chunk c's tiles
+            //     are in, and Y_inter(c-1) = C~_{c-1} G_{c-2} -> TMEM Y_inter, which
+            //     warpgroup 1 needs halfway through chunk c-1
+            if (tid == 0) issue_early(c);
             float d_nx[2] = {0.0f, 0.0f}, l_nx[2] = {1.0f, 1.0f}, dn_nx = 0.0f, ln_nx = 1.0f;
             if (c + 1 < nch) load_scalars(c + 1, d_nx, l_nx, dn_nx, ln_nx);
 
@@ -458,7 +479,6 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (tid == 0) {
                 bool ok = true;
                 if (c >= 1) ok = ptx::mbar_wait(&bar_dgfree, (c - 1) & 1, kWaitBudget);
-                if (!ROT && ok && c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
                 if (!ok) {
                     m3::set_status(m3::kStatusWaitTimeout);
                     abort_s = 1;
@@ -487,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             for (int u = 0; u < 2; ++u) { d_cur[u] = d_nx[u]; l_cur[u] = l_nx[u]; }
             dn_cur = dn_nx; ln_cur = ln_nx;
         }
+        if (tid == 0 && !aborted && nch >= 2) issue_early(nch);   // Y_inter(nch - 1)
     } else {
         // ======================= warpgroup 1: mask, state, output =======================
         const int w1 = warp - 4;
@@ -517,18 +538,6 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             uint32_t v[32];
 #pragma unroll
             for (int J = 0; J < 4; ++J) ptx::tmem_ld16x2_8(tm_sy + 16 * J, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * J]));
-            if (leader && !fail && c > 0) {
-                // Y_inter = C~ G_{c-1} (G: bf16 [N][P] rows, MN-major)
-                const uint32_t c_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_C), 16);
-                const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(t_g), N * 128);
-                constexpr uint32_t id_y = ptx::idesc_bf16(kRows, kP, false, true);
-#pragma unroll
-                for (int k16 = 0; k16 < N / 16; ++k16) {
-                    const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
-                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + CF::TM_YI, c_lo + ko, g_lo + k16 * 128, id_y, k16 > 0);
-                }
-                ptx::umma_commit(&bar_yi);
-            }
             // (2) mask: S' = S o M for this thread's row, 8 columns in each of the
             //     four 16-row blocks; the block kind (below / diagonal / above)
             //     is the same for the whole warp
