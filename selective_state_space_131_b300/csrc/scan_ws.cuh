@@ -55,6 +55,10 @@ constexpr int kP = 64;                          // headdim
 constexpr long long kWaitBudget = 4000000000LL; // clock cycles (~2 s) before a wait gives up
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr uint32_t kBarWG0 = 1, kBarWG1 = 2;
+// Warpgroup 0's MMA issuers, one lane in each of two warps other than warp 0
+// (which computes the chunk scalars), so that no warp carries two serial jobs.
+constexpr int kEarlyIssuer = 32;   // Phi(c), Y_inter(c-1)
+constexpr int kLateIssuer = 64;    // S(c), dG(c)
 // Largest decay span (log2 units) across one 16-row mask block for which the
 // diagonal block is evaluated in factorised form; beyond it, exactly.
 constexpr float kSpanMax = 96.0f;
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_full[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_phi, bar_fin[2];
+    __shared__ uint64_t bar_full[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_phi, bar_fin[3];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
 
@@ -190,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             ptx::mbar_init(&bar_full[s], 1);
             ptx::mbar_init(&bar_sd[s], 1);
             ptx::mbar_init(&bar_syfree[s], 1);
-            ptx::mbar_init(&bar_fin[s], 1);
         }
+        for (int k = 0; k < 3; ++k) ptx::mbar_init(&bar_fin[k], 1);
         ptx::mbar_init(&bar_dgfree, 1);
         ptx::mbar_init(&bar_yi, 1);
         ptx::mbar_init(&bar_y, 1);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         };
         float d_cur[2], l_cur[2], dn_cur, ln_cur;
         load_scalars(0, d_cur, l_cur, dn_cur, ln_cur);
-        // thread 0 only: the MMAs of step (0) for chunk c (c = nch: the last Y_inter)
+        // thread kEarlyIssuer only: the MMAs of step (0) for chunk c (c = nch: the last Y_inter)
         auto issue_early = [&](int c) {
             const int s = c & 1;
             bool ok = true;
@@ -330,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             uint8_t* st = smem + s * CF::ST_BYTES;
             float* sc = scal0 + s * CF::SC_STRIDE;
             const uint32_t tm_sy = tmem + CF::TM_SY0 + 64u * s;
-            // (0) thread 0, once chunk c-2's output has been read (its S/Y buffer and
+            // (0) thread kEarlyIssuer, once chunk c-2's output has been read (its S/Y buffer and
             //     Y_inter free): Phi_rows = L theta -> TMEM S/Y[s] when chunk c's tiles
             //     are in, and Y_inter(c-1) = C~_{c-1} G_{c-2} -> TMEM Y_inter, which
             //     warpgroup 1 needs halfway through chunk c-1
-            if (tid == 0) issue_early(c);
+            if (tid == kEarlyIssuer) issue_early(c);
             float d_nx[2] = {0.0f, 0.0f}, l_nx[2] = {1.0f, 1.0f}, dn_nx = 0.0f, ln_nx = 1.0f;
             if (c + 1 < nch) load_scalars(c + 1, d_nx, l_nx, dn_nx, ln_nx);
 
@@ -475,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (fail) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
             if (ptx::bar_sync_or(kBarWG0, kWG, fail || abort_s)) { aborted = true; break; }
 
-            // (5) thread 0: S = C~ B~^T -> TMEM S/Y[s];  dG = B~'^T X -> TMEM dG
-            if (tid == 0) {
+            // (5) thread kLateIssuer: S = C~ B~^T -> TMEM S/Y[s];  dG = B~'^T X -> TMEM dG
+            if (tid == kLateIssuer) {
                 bool ok = true;
                 if (c >= 1) ok = ptx::mbar_wait(&bar_dgfree, (c - 1) & 1, kWaitBudget);
                 if (!ok) {
@@ -507,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             for (int u = 0; u < 2; ++u) { d_cur[u] = d_nx[u]; l_cur[u] = l_nx[u]; }
             dn_cur = dn_nx; ln_cur = ln_nx;
         }
-        if (tid == 0 && !aborted && nch >= 2) issue_early(nch);   // Y_inter(nch - 1)
+        if (tid == kEarlyIssuer && !aborted && nch >= 2) issue_early(nch);   // Y_inter(nch - 1)
     } else {
         // ======================= warpgroup 1: mask, state, output =======================
         const int w1 = warp - 4;
@@ -738,11 +742,11 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         for (int s = 0; s < 2; ++s)
             if (last_load[s] >= 0) (void)ptx::mbar_wait(&bar_full[s], (last_load[s] >> 1) & 1, kWaitBudget);
     }
-    if (aborted && (tid == 0 || tid == kWG)) {
+    if (aborted && (tid == kEarlyIssuer || tid == kLateIssuer || tid == kWG)) {
         // every MMA this thread issued has completed once this commit arrives
-        const int wg = tid / kWG;
-        ptx::umma_commit(&bar_fin[wg]);
-        (void)ptx::mbar_wait(&bar_fin[wg], 0, kWaitBudget);
+        const int k = (tid == kEarlyIssuer) ? 0 : (tid == kLateIssuer ? 1 : 2);
+        ptx::umma_commit(&bar_fin[k]);
+        (void)ptx::mbar_wait(&bar_fin[k], 0, kWaitBudget);
     }
     ptx::tc_fence_before();
     __syncthreads();
