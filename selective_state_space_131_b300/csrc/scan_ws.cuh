@@ -59,6 +59,9 @@ constexpr uint32_t kBarWG0 = 1, kBarWG1 = 2;
 // (which computes the chunk scalars), so that no warp carries two serial jobs.
 constexpr int kEarlyIssuer = 32;   // Phi(c), Y_inter(c-1)
 constexpr int kLateIssuer = 64;    // S(c), dG(c)
+// Warpgroup 1's serial jobs, likewise one lane in each of three warps.
+constexpr int kYIssuer = 2 * 64 + 32;   // (warp 5) Y_intra(c)
+constexpr int kLoader = 2 * 64 + 64;    // (warp 6) the TMA loads of every chunk
 // Largest decay span (log2 units) across one 16-row mask block for which the
 // diagonal block is evaluated in factorised form; beyond it, exactly.
 constexpr float kSpanMax = 96.0f;
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    // TMA loads of chunk c into stage c % 2 (issued by thread kWG only).
+    // TMA loads of chunk c into stage c % 2 (issued by thread kLoader only).
     auto issue_loads = [&](int c) {
         const int s = c & 1;
         uint8_t* st = smem + s * CF::ST_BYTES;
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         }
         if (ROT) ptx::tma_load_4d(st + CF::ST_TH, &map_th, &bar_full[s], 0, h, t0, b);
     };
-    int last_load[2] = {-1, -1};     // thread kWG only: last chunk loaded into each stage
+    int last_load[2] = {-1, -1};     // thread kLoader only: last chunk loaded into each stage
     bool aborted = false;
     // fp32 chunk state G, rows owned by the consumer threads (M = 64 accumulator
     // layout for N = 64: row 16 w + lane % 16, columns 32 (lane / 16) + [0, 32);
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         const uint32_t lane_base = (uint32_t)(w1 * 32) << 16;
         const int g_row = (N == 64) ? i_row : (w1 * 32 + lane);
 
-        if (leader) {
+        if (tid == kLoader) {
             for (int c = 0; c < 2 && c < nch; ++c) {
                 issue_loads(c);
                 last_load[c] = c;
@@ -632,9 +635,9 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (leader) ptx::bulk_wait_read0();   // the previous y store has left the staging tile
             if (fail) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
             if (ptx::bar_sync_or(kBarWG1, kWG, fail || abort_s)) { aborted = true; break; }
-            if (leader) {
+            if (leader) ptx::mbar_arrive(&bar_dgfree);
+            if (tid == kYIssuer) {
                 ptx::tc_fence_after();
-                ptx::mbar_arrive(&bar_dgfree);
                 // Y_intra = S' X -> TMEM S/Y[s] (S has been read by every thread)
                 const uint32_t sp_lo = ptx::sdesc_lo(ptx::smem_u32(t_sp), 16);
                 const uint32_t x_lo = ptx::sdesc_lo(ptx::smem_u32(st + CF::ST_X), TILE);
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (!fail) fail = !ptx::mbar_wait(&bar_y, c & 1, kWaitBudget);
             __syncwarp();
             ptx::tc_fence_after();
-            if (leader && !fail && c + 2 < nch) {
+            if (tid == kLoader && !fail && c + 2 < nch) {
                 issue_loads(c + 2);
                 last_load[s] = c + 2;
             }
@@ -736,13 +739,13 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             *reinterpret_cast<float4*>(fs + p4 * 4) = make_float4(o[0], o[1], o[2], o[3]);
         }
     }
-    if (aborted && tid == kWG) {
-        // stopped early: wait (bounded) for the stores and loads still in flight
-        ptx::bulk_wait0();
+    if (aborted && tid == kWG) ptx::bulk_wait0();   // y stores still in flight
+    if (aborted && tid == kLoader) {
+        // stopped early: wait (bounded) for the loads still in flight
         for (int s = 0; s < 2; ++s)
             if (last_load[s] >= 0) (void)ptx::mbar_wait(&bar_full[s], (last_load[s] >> 1) & 1, kWaitBudget);
     }
-    if (aborted && (tid == kEarlyIssuer || tid == kLateIssuer || tid == kWG)) {
+    if (aborted && (tid == kEarlyIssuer || tid == kLateIssuer || tid == kYIssuer)) {
         // every MMA this thread issued has completed once this commit arrives
         const int k = (tid == kEarlyIssuer) ? 0 : (tid == kLateIssuer ? 1 : 2);
         ptx::umma_commit(&bar_fin[k]);
