@@ -38,13 +38,13 @@ HBM_FALLBACK_GBS = 6400.0
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # prefill kernel from one ncu capture, keyed by workload, with the sha256 prefix
 # of the kernel source the counters were taken on: reported only while the
-# source is unchanged, else null.  Captured on batch 2 and scaled x4 to batch 8
-# (traffic grows with the number of (batch, head) sequences); the summary with
-# its command is profiles/m3_scan_tc_siso_b2T8192P64N64.md.
+# source is unchanged, else null.  Captured at T = 2048 and scaled x4 to
+# T = 8192 (traffic grows with the sequence length); the summary with its
+# command is profiles/m3_scan_ws_siso_b8T2048P64N64.md.
 NCU_TRAFFIC = {
-    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.131392e6 + 51.497984e6),
+    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.187712e6 + 48.630272e6),
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
-                                      "sha256": "81ee047a047b5f20"},
+                                      "sha256": "cc08b81532d29f7b"},
 }
 
 
