@@ -155,6 +155,29 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0][1], "reasons": reasons, "samples": len(rows)}
 
 
+def rank_seed(workload: int, rank: int) -> int:
+    """Input seed of one rank: every rank draws its own copy of the workload
+    (independent (batch, head) sequences, weak scaling, no data exchanged)."""
+    return workload + 1000 * rank
+
+
+def max_over_ranks(ms: float, world: int, device="cpu") -> float:
+    """The step time the job is charged: the slowest rank's (all_reduce MAX;
+    NCCL on the GPU path, gloo on CPU)."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank in
+    the (max-over-ranks) step time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -331,7 +354,7 @@ def main():
             print(json.dumps(bench_decode(m3, stream, args.decode_steps, rank, rank=r)), flush=True)
         return 0
 
-    inp = inputs.make_scan_inputs(shape, args.workload + 1000 * rank)
+    inp = inputs.make_scan_inputs(shape, rank_seed(args.workload, rank))
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     b, T, H, R, P = d["x"].shape
     N = d["B"].shape[-1]
@@ -365,17 +388,12 @@ def main():
             step()
         e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     if m3.m3_device_status(stream) != m3.M3_OK:
         raise RuntimeError("device status set during the timed region")
 
     tokens = b * T
-    value = world * tokens / (ms * 1e-3)
+    value = whole_job_rate(tokens, world, ms)
     peaks, peak_kind = measured_peaks()
     nbytes = scan_bytes(shape)
     achieved = nbytes / (ms * 1e-3) / 1e9
@@ -424,7 +442,8 @@ def main():
         a1.record(stream)
         barrier()
         ems = a0.elapsed_time(a1) / e_steps
-        result["e2e"] = {"value": world * tokens / (ems * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(ems, world, dev)
+        result["e2e"] = {"value": whole_job_rate(tokens, world, ems), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": e_steps}
 
     del d, y, fs
