@@ -117,6 +117,26 @@ M3_API int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const f
                 void* y, float* final_state, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/* Prefill that continues a sequence: the same computation as m3_scan_fwd,
+ * started from a given state instead of zero (the chunked-prefill continuation
+ * of a serving loop: prefill -> decode -> prefill ...).  With h_{-1} the state
+ * before x's first token and u_{-1} = sum_r prev_B[r] prev_x[r]^T the input of
+ * the token before it, the first token's update is
+ *   h'_0 = Rot(theta_0)(alpha_0 h_{-1} + beta_0 u_{-1}) + gamma_0 u_0
+ * (Mamba-3 summary page §3.1 eq. (5): the previous-token term), and the rest
+ * as in m3_scan_fwd.
+ *   initial_state [b, h, N, P] fp32, complex frame (the frame final_state and
+ *                 m3_step use), 16-byte aligned, or NULL for zero
+ *   prev_B [b, h, R, N], prev_x [b, h, R, P]  dtype: the previous token's B and
+ *                 x, or both NULL (no previous token)
+ * Every other argument as in m3_scan_fwd.  T == 0 copies initial_state (or
+ * zero) to final_state. */
+M3_API int m3_scan_fwd_from(const m3_dims* d, const void* x, const float* dt, const float* A,
+                     const void* B, const void* C, const float* lambda, const void* theta,
+                     const float* initial_state, const void* prev_B, const void* prev_x,
+                     void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
 /* One decode step for every (b, h) (same recurrence, one token):
  *   state   [b, h, N, P]  fp32, read and overwritten with h'_t (complex frame)
  *   x_t     [b, h, R, P]  dtype      dt_t, lambda_t [b, h] fp32 (lambda_t may

@@ -91,27 +91,29 @@ int launch_step(const m3_dims* d, const SimtArgs& a, int block, float* state, co
 template <typename T, int NPT>
 int launch_seq(const m3_dims* d, const SimtArgs& a, int block, const void* x, const float* dt, const float* A,
                const void* B, const void* C, const float* lam, const void* theta, void* y, float* final_state,
-               cudaStream_t s) {
+               const float* h0, const void* prev_B, const void* prev_x, cudaStream_t s) {
     auto k = m3::m3_scan_seq_kernel<T, NPT>;
     const size_t smem = seq_smem_bytes(a);
     int rc = prepare(k, smem);
     if (rc != M3_OK) return rc;
     k<<<(unsigned)(d->batch * d->heads), block, smem, s>>>(a, d->seqlen, d->heads, (const T*)x, dt, A, (const T*)B,
-                                                          (const T*)C, lam, (const T*)theta, (T*)y, final_state);
+                                                          (const T*)C, lam, (const T*)theta, (T*)y, final_state, h0,
+                                                          (const T*)prev_B, (const T*)prev_x);
     return launch_status();
 }
 
 template <typename T>
 int dispatch_seq(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
-                 const float* lam, const void* theta, void* y, float* fs, cudaStream_t s) {
+                 const float* lam, const void* theta, void* y, float* fs, const float* h0, const void* pB,
+                 const void* px, cudaStream_t s) {
     SimtArgs a;
     int npt, block;
     if (!simt_geometry(d, &a, &npt, &block)) return M3_ERR_UNSUPPORTED;
     switch (npt) {
-        case 1: return launch_seq<T, 1>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
-        case 2: return launch_seq<T, 2>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
-        case 4: return launch_seq<T, 4>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
-        case 8: return launch_seq<T, 8>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, s);
+        case 1: return launch_seq<T, 1>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, h0, pB, px, s);
+        case 2: return launch_seq<T, 2>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, h0, pB, px, s);
+        case 4: return launch_seq<T, 4>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, h0, pB, px, s);
+        case 8: return launch_seq<T, 8>(d, a, block, x, dt, A, B, C, lam, theta, y, fs, h0, pB, px, s);
     }
     return M3_ERR_UNSUPPORTED;
 }
@@ -182,9 +184,10 @@ size_t m3_scan_workspace_size(const m3_dims* d) {
 
 int m3_scan_algorithm(const m3_dims* d) { return scan_algorithm(d); }
 
-int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
-                const float* lambda, const void* theta, void* y, float* final_state, void* workspace,
-                size_t workspace_bytes, void* stream) {
+int m3_scan_fwd_from(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                     const float* lambda, const void* theta, const float* initial_state, const void* prev_B,
+                     const void* prev_x, void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                     void* stream) {
     int rc = check_dims(d, true);
     if (rc != M3_OK) return rc;
     (void)workspace;
@@ -192,30 +195,43 @@ int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A
     const bool has_tokens = d->batch > 0 && d->seqlen > 0;
     if (has_tokens && (!x || !dt || !A || !B || !C || !y)) return M3_ERR_NULL;
     if (d->batch > 0 && !A) return M3_ERR_NULL;
+    if ((prev_B == nullptr) != (prev_x == nullptr)) return M3_ERR_NULL;
     const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
-    const void* elem_ptrs[] = {x, B, C, theta, y};
+    const void* elem_ptrs[] = {x, B, C, theta, y, prev_B, prev_x};
     for (const void* p : elem_ptrs)
         if (p && !aligned(p, es)) return M3_ERR_ALIGN;
     const void* f32_ptrs[] = {dt, A, lambda};
     for (const void* p : f32_ptrs)
         if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
     if (final_state && !aligned16(final_state)) return M3_ERR_ALIGN;
+    if (initial_state && !aligned16(initial_state)) return M3_ERR_ALIGN;
     const int algo = scan_algorithm(d);
     if (algo == M3_ALGO_NONE) return M3_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d->batch == 0) return M3_OK;
+    const size_t state_bytes = sizeof(float) * d->batch * d->heads * d->dstate * d->headdim;
     if (d->seqlen == 0) {
-        if (final_state &&
-            cudaMemsetAsync(final_state, 0, sizeof(float) * d->batch * d->heads * d->dstate * d->headdim, s) !=
-                cudaSuccess)
-            return M3_ERR_CUDA;
-        return M3_OK;
+        // no token: the state passes through unchanged (the previous token's
+        // input is carried by the caller, not folded into the state)
+        if (!final_state) return M3_OK;
+        const cudaError_t e = initial_state
+                                  ? cudaMemcpyAsync(final_state, initial_state, state_bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(final_state, 0, state_bytes, s);
+        return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
     }
     if (algo == M3_ALGO_CHUNKED_TC)
-        return m3ws::launch(*d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+        return m3ws::launch(*d, x, dt, A, B, C, lambda, theta, initial_state, prev_B, prev_x, y, final_state, s);
     if (d->dtype == M3_F32)
-        return dispatch_seq<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);
-    return dispatch_seq<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, s);
+        return dispatch_seq<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state, prev_B, prev_x, s);
+    return dispatch_seq<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state, prev_B, prev_x,
+                                       s);
+}
+
+int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                const float* lambda, const void* theta, void* y, float* final_state, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    return m3_scan_fwd_from(d, x, dt, A, B, C, lambda, theta, nullptr, nullptr, nullptr, y, final_state, workspace,
+                            workspace_bytes, stream);
 }
 
 int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A, const void* B_t,

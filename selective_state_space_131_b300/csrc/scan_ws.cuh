@@ -117,6 +117,11 @@ struct Params {
     const float* A;
     const float* lam;    // may be null (lambda = 1)
     float* final_state;  // may be null
+    // continuation (all may be null): the state before the first token (complex
+    // frame, fp32 [b, h, N, P]) and the token before it (bf16 [b, h, R, N] / [b, h, R, P])
+    const float* h0;
+    const __nv_bfloat16* prev_B;
+    const __nv_bfloat16* prev_x;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -211,6 +216,45 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         ptx::tmem_relinquish();
     }
     if (tid < 2 * K) s_carry[tid] = 0.0f;
+    // fp32 chunk state G, rows owned by the consumer threads (M = 64 accumulator
+    // layout for N = 64: row 16 w + lane % 16, columns 32 (lane / 16) + [0, 32);
+    // M = 128 layout for N = 128: row 32 w + lane, all 64 columns)
+    constexpr int GC = (N == 64) ? 32 : 64;
+    float G[GC];
+#pragma unroll
+    for (int p = 0; p < GC; ++p) G[p] = 0.0f;
+    // A continuation starts from the augmented state G_{-1} = h_{-1} + (1 - lambda_0)
+    // dt_0 prev_B^T prev_x (the RoPE frame of this call starts at angle 0, so the
+    // complex-frame state is also the rotated-frame state); warpgroup 1 holds it in
+    // its fp32 registers and puts the bf16 copy Y_inter(0) reads in shared memory.
+    const bool has_init = (prm.h0 != nullptr) || (prm.prev_B != nullptr);
+    if (has_init && tid >= kWG && tid < 2 * kWG) {
+        const int w1 = warp - 4;
+        const int g_row = (N == 64) ? (w1 * 16 + (lane & 15)) : (w1 * 32 + lane);
+        const int col0 = (N == 64) ? (lane >> 4) * 32 : 0;
+        const int64_t i0 = ((int64_t)b * T) * prm.H + h;             // token 0 of this (b, h)
+        const float d0 = T > 0 ? __ldg(prm.dt + i0) : 0.0f;
+        const float l0 = (T > 0 && prm.lam) ? __ldg(prm.lam + i0) : 1.0f;
+        const float bcoef = (1.0f - l0) * d0;
+        const int64_t uh = (int64_t)b * prm.H + h;
+#pragma unroll
+        for (int p = 0; p < GC; ++p) {
+            float v = prm.h0 ? __ldg(prm.h0 + (uh * N + g_row) * kP + col0 + p) : 0.0f;
+            if (prm.prev_B) {
+                float u = 0.0f;
+                for (int r = 0; r < R; ++r)
+                    u = fmaf(__bfloat162float(prm.prev_B[(uh * R + r) * N + g_row]),
+                             __bfloat162float(prm.prev_x[(uh * R + r) * kP + col0 + p]), u);
+                v = fmaf(bcoef, u, v);
+            }
+            G[p] = v;
+        }
+#pragma unroll
+        for (int g = 0; g < GC / 8; ++g)
+            *reinterpret_cast<uint4*>(t_g + swz(g_row, col0 / 8 + g)) =
+                make_uint4(pack_bf16(G[g * 8 + 0], G[g * 8 + 1]), pack_bf16(G[g * 8 + 2], G[g * 8 + 3]),
+                           pack_bf16(G[g * 8 + 4], G[g * 8 + 5]), pack_bf16(G[g * 8 + 6], G[g * 8 + 7]));
+    }
     // L[i][t] = 1 for t <= token(i) = i / R (and t < Q), else 0: 64 x 64 bf16, 128-byte swizzle
     for (int e = tid; e < kRows * 8; e += kThreads) {
         const int i = e >> 3, g = e & 7;
@@ -246,13 +290,6 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     };
     int last_load[2] = {-1, -1};     // thread kLoader only: last chunk loaded into each stage
     bool aborted = false;
-    // fp32 chunk state G, rows owned by the consumer threads (M = 64 accumulator
-    // layout for N = 64: row 16 w + lane % 16, columns 32 (lane / 16) + [0, 32);
-    // M = 128 layout for N = 128: row 32 w + lane, all 64 columns)
-    constexpr int GC = (N == 64) ? 32 : 64;
-    float G[GC];
-#pragma unroll
-    for (int p = 0; p < GC; ++p) G[p] = 0.0f;
 
     if (tid < kWG) {
         // ======================= warpgroup 0: prologue + S / dG issue =======================
@@ -317,8 +354,9 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                                                        th_lo + k16 * (CF::TH_K16 >> 4), id_phi, k16 > 0);
                 ptx::umma_commit(&bar_phi);
             }
-            if (c >= 2) {
-                // Y_inter(c-1) = C~_{c-1} G_{c-2} (G: bf16 [N][P] rows, MN-major)
+            if (c >= 2 || (c == 1 && (prm.h0 != nullptr || prm.prev_B != nullptr))) {
+                // Y_inter(c-1) = C~_{c-1} G_{c-2} (G: bf16 [N][P] rows, MN-major; G_{-1}
+                // is the continuation's initial state)
                 const uint32_t c_lo =
                     ptx::sdesc_lo(ptx::smem_u32(smem + ((c - 1) & 1) * CF::ST_BYTES + CF::ST_C), 16);
                 const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(t_g), N * 128);
@@ -514,7 +552,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             for (int u = 0; u < 2; ++u) { d_cur[u] = d_nx[u]; l_cur[u] = l_nx[u]; }
             dn_cur = dn_nx; ln_cur = ln_nx;
         }
-        if (tid == kEarlyIssuer && !aborted && nch >= 2) issue_early(nch);   // Y_inter(nch - 1)
+        if (tid == kEarlyIssuer && !aborted && (nch >= 2 || prm.h0 != nullptr || prm.prev_B != nullptr))
+            issue_early(nch);   // Y_inter(nch - 1)
     } else {
         // ======================= warpgroup 1: mask, state, output =======================
         const int w1 = warp - 4;
@@ -650,7 +689,11 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }
             // (4) G_{c-1} is no longer read: store the bf16 copy of G_c
             fail = false;
-            if (c > 0) fail = !ptx::mbar_wait(&bar_yi, (c - 1) & 1, kWaitBudget);
+            // chunk c has an inter-chunk term (always for a continuation); the flag is
+            // re-read from the kernel parameters rather than kept in a register
+            const bool cont = (prm.h0 != nullptr) || (prm.prev_B != nullptr);
+            const bool has_yi = (c > 0) || cont;
+            if (has_yi) fail = !ptx::mbar_wait(&bar_yi, (cont ? c : c - 1) & 1, kWaitBudget);
             if constexpr (N == 64) {
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
@@ -679,14 +722,14 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 for (int q = 0; q < 2; ++q) {
                     uint32_t ya[16], yb[16];
                     ptx::tmem_ld16x2_16(tm_sy + q * 16, ya);
-                    if (c > 0) ptx::tmem_ld16x2_16(tmem + lane_base + CF::TM_YI + q * 16, yb);
+                    if (has_yi) ptx::tmem_ld16x2_16(tmem + lane_base + CF::TM_YI + q * 16, yb);
                     ptx::tmem_ld_wait();
                     float y[16];
 #pragma unroll
                     for (int j = 0; j < 16; j += 2) {
                         const float2 a2 = make_float2(__uint_as_float(ya[j]), __uint_as_float(ya[j + 1]));
                         float2 r2 = a2;
-                        if (c > 0)
+                        if (has_yi)
                             r2 = __ffma2_rn(make_float2(e, e), make_float2(__uint_as_float(yb[j]), __uint_as_float(yb[j + 1])),
                                             a2);
                         y[j] = r2.x; y[j + 1] = r2.y;
@@ -840,7 +883,8 @@ int launch_r(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cudaS
 }
 
 inline int launch(const m3_dims& d, const void* x, const float* dt, const float* A, const void* B, const void* C,
-                  const float* lam, const void* theta, void* y, float* final_state, cudaStream_t s) {
+                  const float* lam, const void* theta, const float* h0, const void* prev_B, const void* prev_x,
+                  void* y, float* final_state, cudaStream_t s) {
     if (!supports(d)) return M3_ERR_UNSUPPORTED;
     const void* tma_ptrs[] = {x, B, C, theta, y};
     for (const void* p : tma_ptrs)
@@ -863,6 +907,9 @@ inline int launch(const m3_dims& d, const void* x, const float* dt, const float*
     prm.A = A;
     prm.lam = lam;
     prm.final_state = final_state;
+    prm.h0 = h0;
+    prm.prev_B = static_cast<const __nv_bfloat16*>(prev_B);
+    prm.prev_x = static_cast<const __nv_bfloat16*>(prev_x);
     if (d.dstate == 64) return rot ? launch_r<1, true>(d, maps, prm, s) : launch_r<1, false>(d, maps, prm, s);
     return rot ? launch_r<2, true>(d, maps, prm, s) : launch_r<2, false>(d, maps, prm, s);
 }

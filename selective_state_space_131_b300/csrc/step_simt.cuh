@@ -242,7 +242,10 @@ __global__ void __launch_bounds__(512) m3_scan_seq_kernel(SimtArgs a, int64_t T_
                                                           const T* __restrict__ Bm, const T* __restrict__ Cm,
                                                           const float* __restrict__ lam,
                                                           const T* __restrict__ theta, T* __restrict__ y,
-                                                          float* __restrict__ final_state) {
+                                                          float* __restrict__ final_state,
+                                                          const float* __restrict__ h0,
+                                                          const T* __restrict__ prev_B,
+                                                          const T* __restrict__ prev_x) {
     extern __shared__ __align__(16) float smem[];
     const TokLayout L(a.R, a.P, a.N);
     float* tok[3] = {smem, smem + L.size, smem + 2 * L.size};
@@ -269,8 +272,16 @@ __global__ void __launch_bounds__(512) m3_scan_seq_kernel(SimtArgs a, int64_t T_
         return s;
     };
 
-    // token -1: zero (no previous input); token 0 loaded synchronously
+    // token -1: the previous token's x and B of a continuation (zero for a fresh
+    // sequence); token 0 loaded synchronously
     for (int e = threadIdx.x; e < L.size; e += blockDim.x) tok[2][e] = 0.0f;
+    __syncthreads();
+    if (prev_B) {
+        for (int e = threadIdx.x; e < a.R * a.P; e += blockDim.x)
+            tok[2][L.x + e] = IO<T>::ld(prev_x + unit * a.R * a.P, e);
+        for (int e = threadIdx.x; e < a.R * a.N; e += blockDim.x)
+            tok[2][L.B + e] = IO<T>::ld(prev_B + unit * a.R * a.N, e);
+    }
     if (T_len > 0) {
         const TokSource<T> s0 = source(0);
         for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -282,9 +293,12 @@ __global__ void __launch_bounds__(512) m3_scan_seq_kernel(SimtArgs a, int64_t T_
 #pragma unroll
     for (int i = 0; i < NPT; ++i)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) h[i][rr][j] = 0.0f;
+        for (int rr = 0; rr < 2; ++rr) {
+            const int k = tk + i * a.TK;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (h0) v = __ldg(reinterpret_cast<const float4*>(h0 + (unit * a.N + 2 * k + rr) * (int64_t)a.P + 4 * q));
+            h[i][rr][0] = v.x; h[i][rr][1] = v.y; h[i][rr][2] = v.z; h[i][rr][3] = v.w;
+        }
 
     for (int64_t t = 0; t < T_len; ++t) {
         float* cur = tok[t % 3];

@@ -41,6 +41,8 @@ _lib.m3_scan_algorithm.argtypes = [_dp]
 _lib.m3_scan_algorithm.restype = ctypes.c_int
 _lib.m3_scan_fwd.argtypes = [_dp] + [_vp] * 10 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_fwd.restype = ctypes.c_int
+_lib.m3_scan_fwd_from.argtypes = [_dp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
+_lib.m3_scan_fwd_from.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
 _lib.m3_device_status.argtypes = [_vp]
@@ -124,6 +126,20 @@ def m3_scan_fwd(x, dt, A, B, C, lam, theta, y, final_state, chunk: int = 64, wor
         raise M3Error(rc, "m3_scan_fwd")
 
 
+def m3_scan_fwd_from(x, dt, A, B, C, lam, theta, initial_state, prev_B, prev_x, y, final_state, chunk: int = 64,
+                     workspace=None, workspace_bytes: int = 0, stream=None, dims: m3_dims | None = None) -> None:
+    """Prefill continuing a sequence from initial_state [b,h,N,P] (fp32, complex
+    frame; None for zero) and the previous token's prev_B [b,h,R,N] / prev_x
+    [b,h,R,P] (both None for no previous token).  Raises M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, chunk)
+    rc = _lib.m3_scan_fwd_from(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam),
+                               _ptr(theta), _ptr(initial_state), _ptr(prev_B), _ptr(prev_x), _ptr(y),
+                               _ptr(final_state), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_scan_fwd_from")
+
+
 def m3_step(state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, stream=None,
             dims: m3_dims | None = None) -> None:
     """One decode step; updates state in place and writes y_t.  Raises M3Error."""
@@ -144,6 +160,14 @@ def raw_scan_fwd(dims: m3_dims, ptrs, stream=None) -> int:
     workspace, workspace_bytes); returns the status code."""
     *p, ws_bytes = ptrs
     return int(_lib.m3_scan_fwd(ctypes.byref(dims), *p, int(ws_bytes), stream))
+
+
+def raw_scan_fwd_from(dims: m3_dims, ptrs, stream=None) -> int:
+    """Direct call with raw addresses (x, dt, A, B, C, lam, theta, initial_state,
+    prev_B, prev_x, y, final_state, workspace, workspace_bytes); returns the
+    status code."""
+    *p, ws_bytes = ptrs
+    return int(_lib.m3_scan_fwd_from(ctypes.byref(dims), *p, int(ws_bytes), stream))
 
 
 def raw_step(dims: m3_dims, ptrs, stream=None) -> int:

@@ -107,3 +107,19 @@ def test_launch_without_gpu_reports_cuda_error(m3):
         pytest.skip("a GPU is present: fake pointers must not reach a kernel")
     assert m3.raw_scan_fwd(_dims(m3, dtype=m3.M3_F32), _scan_ptrs()) == m3.M3_ERR_CUDA
     assert m3.raw_step(_dims(m3), _step_ptrs()) == m3.M3_ERR_CUDA
+
+
+def _from_ptrs(**over):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, lam=FAKE, theta=FAKE, h0=FAKE, pB=FAKE, px=FAKE, y=FAKE,
+             fs=FAKE, ws=None, wsb=0)
+    p.update(over)
+    return [p[k] for k in ("x", "dt", "A", "B", "C", "lam", "theta", "h0", "pB", "px", "y", "fs", "ws", "wsb")]
+
+
+def test_scan_from_validation(m3):
+    assert m3.raw_scan_fwd_from(_dims(m3), _from_ptrs(pB=None)) == m3.M3_ERR_NULL   # prev_B / prev_x pair
+    assert m3.raw_scan_fwd_from(_dims(m3), _from_ptrs(px=None)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_fwd_from(_dims(m3), _from_ptrs(h0=FAKE + 4)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd_from(_dims(m3), _from_ptrs(pB=FAKE + 1)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd_from(_dims(m3, dstate=7), _from_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd_from(_dims(m3, batch=0), _from_ptrs(x=None, y=None)) == m3.M3_OK
