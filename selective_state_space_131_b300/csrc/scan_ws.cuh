@@ -97,7 +97,10 @@ struct Cfg {
                          SC_DEC = 6 * Q;
     static constexpr int SC_STRIDE = 6 * Q + 4;               // floats per stage
     static constexpr int OFF_CARRY = align16(OFF_SC + 2 * SC_STRIDE * 4);  // float [2][K]: angle carry
-    static constexpr int SMEM_BYTES = OFF_CARRY + 2 * K * 4 + 1024;    // + alignment slack
+    // dt and lambda of a chunk's Q tokens and the token after it, per stage: float [2][2][DL]
+    static constexpr int DL = (Q + 1 + 3) & ~3;
+    static constexpr int OFF_DL = OFF_CARRY + 2 * K * 4;
+    static constexpr int SMEM_BYTES = OFF_DL + 2 * 2 * DL * 4 + 1024;  // + alignment slack
     // theta tile [Q][K] as the MN-major B operand of Phi = L theta: 64-byte
     // swizzle for K = 32 pairs, 128-byte swizzle for K = 64
     static constexpr uint32_t TH_SBO = (K == 32) ? 512 : 1024;
@@ -308,29 +311,21 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         const int hf = lane >> 4;
         const int tok = row / R;
         float* carry_buf = reinterpret_cast<float*>(smem + CF::OFF_CARRY);   // [2][K]
-        // dt / lambda of tokens c0 + lane, c0 + 32 + lane and c0 + Q, one chunk ahead
-        auto load_scalars = [&](int c, float (&dv)[2], float (&lv)[2], float& dn, float& ln) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int tt = u * 32 + lane;
+        // warp 0 only: dt / lambda of chunk c's tokens and of the token after it
+        // (zero past the end), copied into shared memory one chunk ahead
+        float* s_dl = reinterpret_cast<float*>(smem + CF::OFF_DL);   // [stage][dt | lambda][DL]
+        auto prefetch_scalars = [&](int c) {
+            float* dst = s_dl + (c & 1) * 2 * CF::DL;
+            for (int tt = lane; tt <= Q; tt += 32) {
                 const int64_t t = (int64_t)c * Q + tt;
-                dv[u] = 0.0f; lv[u] = 1.0f;
-                if (tt < Q && t < T) {
-                    const int64_t idx = ((int64_t)b * T + t) * prm.H + h;
-                    dv[u] = __ldg(prm.dt + idx);
-                    if (prm.lam) lv[u] = __ldg(prm.lam + idx);
-                }
+                const bool ok = t < T;
+                const int64_t idx = ok ? ((int64_t)b * T + t) * prm.H + h : 0;
+                ptx::cp_async4(dst + tt, prm.dt + idx, ok);
+                if (prm.lam) ptx::cp_async4(dst + CF::DL + tt, prm.lam + idx, ok);
             }
-            const int64_t tn = (int64_t)(c + 1) * Q;
-            dn = 0.0f; ln = 1.0f;
-            if (tn < T) {
-                const int64_t idx = ((int64_t)b * T + tn) * prm.H + h;
-                dn = __ldg(prm.dt + idx);
-                if (prm.lam) ln = __ldg(prm.lam + idx);
-            }
+            ptx::cp_async_commit();
         };
-        float d_cur[2], l_cur[2], dn_cur, ln_cur;
-        load_scalars(0, d_cur, l_cur, dn_cur, ln_cur);
+        if (warp == 0) prefetch_scalars(0);
         // thread kEarlyIssuer only: the MMAs of step (0) for chunk c (c = nch: the last Y_inter)
         auto issue_early = [&](int c) {
             const int s = c & 1;
@@ -380,26 +375,25 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             //     are in, and Y_inter(c-1) = C~_{c-1} G_{c-2} -> TMEM Y_inter, which
             //     warpgroup 1 needs halfway through chunk c-1
             if (tid == kEarlyIssuer) issue_early(c);
-            float d_nx[2] = {0.0f, 0.0f}, l_nx[2] = {1.0f, 1.0f}, dn_nx = 0.0f, ln_nx = 1.0f;
-            if (c + 1 < nch) load_scalars(c + 1, d_nx, l_nx, dn_nx, ln_nx);
 
             // (1) warp 0: chunk scalars for tokens lane (u = 0) and 32 + lane (u = 1):
             //     cs (log2 units), gamma, w, B~' row scale, mask column weights
             if (warp == 0) {
-                float dnext[2], lnext[2];
-                {
-                    const float d0s = __shfl_down_sync(0xffffffffu, d_cur[0], 1);
-                    const float l0s = __shfl_down_sync(0xffffffffu, l_cur[0], 1);
-                    const float d1s = __shfl_down_sync(0xffffffffu, d_cur[1], 1);
-                    const float l1s = __shfl_down_sync(0xffffffffu, l_cur[1], 1);
-                    const float d1f = __shfl_sync(0xffffffffu, d_cur[1], 0);
-                    const float l1f = __shfl_sync(0xffffffffu, l_cur[1], 0);
-                    if (lane + 1 < Q && lane < 31) { dnext[0] = d0s; lnext[0] = l0s; }
-                    else if (lane + 1 == Q) { dnext[0] = dn_cur; lnext[0] = ln_cur; }
-                    else if (lane == 31 && Q > 32) { dnext[0] = d1f; lnext[0] = l1f; }
-                    else { dnext[0] = 0.0f; lnext[0] = 1.0f; }       // padding rows of a short chunk
-                    dnext[1] = (lane < 31) ? d1s : dn_cur;
-                    lnext[1] = (lane < 31) ? l1s : ln_cur;
+                ptx::cp_async_wait_all();   // this chunk's dt / lambda (copied during chunk c-1)
+                __syncwarp();
+                if (c + 1 < nch) prefetch_scalars(c + 1);
+                const float* sdt = s_dl + s * 2 * CF::DL;
+                const float* slm = sdt + CF::DL;
+                float d_cur[2], l_cur[2], dnext[2], lnext[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    // token t = 32 u + lane and the one after it (t + 1 <= Q wherever used)
+                    const int t = u * 32 + lane;
+                    const bool in = t < Q;
+                    d_cur[u] = in ? sdt[t] : 0.0f;
+                    dnext[u] = in ? sdt[t + 1] : 0.0f;
+                    l_cur[u] = (in && prm.lam) ? slm[t] : 1.0f;
+                    lnext[u] = (in && prm.lam) ? slm[t + 1] : 1.0f;
                 }
                 float cs[2];
 #pragma unroll
@@ -548,12 +542,10 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     ptx::umma_commit(&bar_sd[s]);
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) { d_cur[u] = d_nx[u]; l_cur[u] = l_nx[u]; }
-            dn_cur = dn_nx; ln_cur = ln_nx;
         }
         if (tid == kEarlyIssuer && !aborted && (nch >= 2 || prm.h0 != nullptr || prm.prev_B != nullptr))
             issue_early(nch);   // Y_inter(nch - 1)
+        if (warp == 0) ptx::cp_async_wait_all();   // a stop may leave a scalar copy in flight
     } else {
         // ======================= warpgroup 1: mask, state, output =======================
         const int w1 = warp - 4;
