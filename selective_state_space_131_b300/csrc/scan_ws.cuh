@@ -86,7 +86,12 @@ struct Cfg {
     static constexpr int ST_TH = ST_C + NSLAB * TILE;
     static constexpr int TH_BYTES = ROT ? Q * K * 2 : 0;
     static constexpr int ST_BYTES = align1k(ST_TH + TH_BYTES);
-    static constexpr uint32_t TX_BYTES = TILE * (1 + 2 * NSLAB) + TH_BYTES;
+    // With the rotation, a stage fills in two parts: theta and B, which the
+    // prologue needs first and which are free again once S has been computed,
+    // then C and x, free once Y_inter and Y_intra have been computed.  Without
+    // it, the prologue needs all tiles at once and part a carries them all.
+    static constexpr uint32_t TX_A = ROT ? TILE * NSLAB + TH_BYTES : TILE * (1 + 2 * NSLAB);
+    static constexpr uint32_t TX_B = TILE * (1 + NSLAB);
     static constexpr int OFF_BD = 2 * ST_BYTES;               // B~' (2 stages)
     static constexpr int OFF_SP = OFF_BD + 2 * NSLAB * TILE;  // S' (K-major)
     static constexpr int OFF_G = OFF_SP + TILE;               // G bf16 [N][P] (MN-major)
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_full[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_phi, bar_fin[3];
+    __shared__ uint64_t bar_lda[2], bar_ldb[2], bar_sd[2], bar_syfree[2], bar_dgfree, bar_yi, bar_y, bar_phi, bar_fin[3];
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
 
@@ -202,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&bar_full[s], 1);
+            ptx::mbar_init(&bar_lda[s], 1);
+            ptx::mbar_init(&bar_ldb[s], 1);
             ptx::mbar_init(&bar_sd[s], 1);
             ptx::mbar_init(&bar_syfree[s], 1);
         }
@@ -277,21 +283,33 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    // TMA loads of chunk c into stage c % 2 (issued by thread kLoader only).
-    auto issue_loads = [&](int c) {
+    // TMA loads of chunk c into stage c % 2 (issued by thread kLoader only):
+    // part a (theta and B; every tile without the rotation) and part b (C and x)
+    auto issue_loads_a = [&](int c) {
         const int s = c & 1;
         uint8_t* st = smem + s * CF::ST_BYTES;
         const int t0 = c * Q;
-        ptx::mbar_arrive_expect_tx(&bar_full[s], CF::TX_BYTES);
-        ptx::tma_load_5d(st + CF::ST_X, &map_x, &bar_full[s], 0, 0, h, t0, b);
+        ptx::mbar_arrive_expect_tx(&bar_lda[s], CF::TX_A);
+        if (ROT) ptx::tma_load_4d(st + CF::ST_TH, &map_th, &bar_lda[s], 0, h, t0, b);
 #pragma unroll
         for (int sl = 0; sl < NSLAB; ++sl) {
-            ptx::tma_load_5d(st + CF::ST_B + sl * TILE, &map_B, &bar_full[s], sl * 64, 0, h, t0, b);
-            ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_full[s], sl * 64, 0, h, t0, b);
+            ptx::tma_load_5d(st + CF::ST_B + sl * TILE, &map_B, &bar_lda[s], sl * 64, 0, h, t0, b);
+            if (!ROT) ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_lda[s], sl * 64, 0, h, t0, b);
         }
-        if (ROT) ptx::tma_load_4d(st + CF::ST_TH, &map_th, &bar_full[s], 0, h, t0, b);
+        if (!ROT) ptx::tma_load_5d(st + CF::ST_X, &map_x, &bar_lda[s], 0, 0, h, t0, b);
     };
-    int last_load[2] = {-1, -1};     // thread kLoader only: last chunk loaded into each stage
+    auto issue_loads_b = [&](int c) {
+        if (!ROT) return;
+        const int s = c & 1;
+        uint8_t* st = smem + s * CF::ST_BYTES;
+        const int t0 = c * Q;
+        ptx::mbar_arrive_expect_tx(&bar_ldb[s], CF::TX_B);
+#pragma unroll
+        for (int sl = 0; sl < NSLAB; ++sl)
+            ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_ldb[s], sl * 64, 0, h, t0, b);
+        ptx::tma_load_5d(st + CF::ST_X, &map_x, &bar_ldb[s], 0, 0, h, t0, b);
+    };
+    int last_a = -1, last_b = -1;   // thread kLoader only: the last chunk of each part loaded
     bool aborted = false;
 
     if (tid < kWG) {
@@ -331,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             const int s = c & 1;
             bool ok = true;
             if (c >= 2) ok = ptx::mbar_wait(&bar_syfree[s], ((c >> 1) - 1) & 1, kWaitBudget);
-            if (ok && ROT && c < nch) ok = ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
+            if (ok && ROT && c < nch) ok = ptx::mbar_wait(&bar_lda[s], (c >> 1) & 1, kWaitBudget);
             if (!ok) {
                 m3::set_status(m3::kStatusWaitTimeout);
                 abort_s = 1;
@@ -431,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }
 
             // (2) this chunk's tiles; the angles of this thread's row and pairs
-            bool fail = !ptx::mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitBudget);
+            bool fail = !ptx::mbar_wait(&bar_lda[s], (c >> 1) & 1, kWaitBudget);
             float cn[PH], sn[PH];
             if (ROT) {
                 if (!fail) fail = !ptx::mbar_wait(&bar_phi, c & 1, kWaitBudget);
@@ -472,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) vb[g] = *reinterpret_cast<const uint4*>(sb + swz(row, hf * GPT + g));
                 if (ROT) {
+                    if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
                     uint4 vc[GPT];
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
@@ -558,8 +577,9 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 
         if (tid == kLoader) {
             for (int c = 0; c < 2 && c < nch; ++c) {
-                issue_loads(c);
-                last_load[c] = c;
+                issue_loads_a(c);
+                issue_loads_b(c);
+                last_a = last_b = c;
             }
         }
         for (int c = 0; c < nch; ++c) {
@@ -571,6 +591,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             bool fail = !ptx::mbar_wait(&bar_sd[s], (c >> 1) & 1, kWaitBudget);
             __syncwarp();   // tcgen05.ld / wait::ld below are warp-aligned
             ptx::tc_fence_after();
+            // theta and B of stage s have been read (Phi_c before S_c; S_c is done):
+            // part a of chunk c + 2
+            if (ROT && tid == kLoader && !fail && c + 2 < nch) {
+                issue_loads_a(c + 2);
+                last_a = c + 2;
+            }
             // S_c, block J (columns 16 J + [0, 16)) in v[8 J, 8 J + 8): this thread
             // holds columns 16 J + 8 hc + [0, 8) (waited for in the mask below)
             uint32_t v[32];
@@ -699,13 +725,19 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                         make_uint4(pack_bf16(G[g * 8 + 0], G[g * 8 + 1]), pack_bf16(G[g * 8 + 2], G[g * 8 + 3]),
                                    pack_bf16(G[g * 8 + 4], G[g * 8 + 5]), pack_bf16(G[g * 8 + 6], G[g * 8 + 7]));
             }
-            // (5) Y_intra done: stage s is free -> TMA of chunk c + 2
+            // (5) Y_intra done: C and x of stage s are free -> part b of chunk c + 2
+            //     (without the rotation, every tile of chunk c + 2)
             if (!fail) fail = !ptx::mbar_wait(&bar_y, c & 1, kWaitBudget);
             __syncwarp();
             ptx::tc_fence_after();
             if (tid == kLoader && !fail && c + 2 < nch) {
-                issue_loads(c + 2);
-                last_load[s] = c + 2;
+                if (ROT) {
+                    issue_loads_b(c + 2);
+                    last_b = c + 2;
+                } else {
+                    issue_loads_a(c + 2);
+                    last_a = c + 2;
+                }
             }
             // (6) y = Y_intra + exp(cs) Y_inter -> bf16 staging -> TMA store
             {
@@ -777,8 +809,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     if (aborted && tid == kWG) ptx::bulk_wait0();   // y stores still in flight
     if (aborted && tid == kLoader) {
         // stopped early: wait (bounded) for the loads still in flight
-        for (int s = 0; s < 2; ++s)
-            if (last_load[s] >= 0) (void)ptx::mbar_wait(&bar_full[s], (last_load[s] >> 1) & 1, kWaitBudget);
+        // (the two stages last received chunks last - 1 and last of each part)
+        for (int k = 0; k < 2; ++k) {
+            const int ca = last_a - k, cb = last_b - k;
+            if (ca >= 0) (void)ptx::mbar_wait(&bar_lda[ca & 1], (ca >> 1) & 1, kWaitBudget);
+            if (ROT && cb >= 0) (void)ptx::mbar_wait(&bar_ldb[cb & 1], (cb >> 1) & 1, kWaitBudget);
+        }
     }
     if (aborted && (tid == kEarlyIssuer || tid == kLateIssuer || tid == kYIssuer)) {
         // every MMA this thread issued has completed once this commit arrives
