@@ -78,6 +78,24 @@ def test_fast_step_shapes(m3, P, N, R, dtype):
     assert ey <= TOL[dtype] and es <= TOL[dtype], (ey, es)
 
 
+# 8192 (b, h) units, several waves of CTAs for every fast shape; sampled units
+# are checked against the oracle.
+@pytest.mark.parametrize("P,N", [pn for pn in FAST if (pn[0] // 4) * (pn[1] // 8) >= 32], ids=lambda v: str(v))
+@pytest.mark.parametrize("R", [1, 2, 4])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fast_step_many_units(m3, P, N, R, dtype):
+    shape = inputs.DecodeShape(batch=256, heads=32, headdim=P, dstate=N, rank=R, steps=3, dtype=dtype)
+    ey, es = run_chain(m3, shape, 200 + P + N + R, 3, sel=([0, 131, 255], [0, 13, 31]))
+    assert ey <= TOL[dtype] and es <= TOL[dtype], (ey, es)
+
+
+def test_fast_step_many_units_optional_inputs(m3):
+    shape = inputs.DecodeShape(batch=256, heads=32, headdim=64, dstate=64, rank=2, steps=3, dtype="f32")
+    ey, es = run_chain(m3, shape, 9, 3, with_prev=False, with_lam=False, with_theta=False,
+                       sel=([1, 254], [2, 30]))
+    assert ey <= 1e-4 and es <= 1e-4, (ey, es)
+
+
 @pytest.mark.parametrize("prev,lam,theta", [(False, True, True), (True, False, True), (True, True, False),
                                             (False, False, False)])
 def test_fast_step_optional_inputs(m3, prev, lam, theta):
