@@ -12,6 +12,8 @@ in ``m3_oracle.c`` (Mamba-3 summary page, §3.1 eq. (5)-(6), §3.2
 Proposition 3.2.1, §3.3 MIMO).  ``forms`` holds independently written
 alternative forms (RoPE frame, quadratic semiseparable mask, width-2
 convolution, MIMO as R^2 SISO systems, complex arithmetic) used as pins.
+``bcnorm`` is the B / C normalisation and bias of the Mamba-3 block (§3.4),
+applied to B and C before the scan.
 """
 from __future__ import annotations
 
