@@ -83,6 +83,7 @@ typedef struct {
 #define M3_ERR_UNSUPPORTED (-6) /* valid sizes this build has no kernel for */
 #define M3_ERR_DEVICE (-7)      /* the device status word was set */
 #define M3_ERR_WORKSPACE (-8)   /* workspace too small */
+#define M3_ERR_VALUE (-9)       /* a scalar argument is out of range (e.g. a negative epsilon) */
 
 /* Prefill algorithms (what m3_scan_fwd would run for given dims). */
 #define M3_ALGO_NONE (-1)       /* no kernel for these dims */
@@ -136,6 +137,29 @@ M3_API int m3_scan_fwd_from(const m3_dims* d, const void* x, const float* dt, co
                      const float* initial_state, const void* prev_B, const void* prev_x,
                      void* y, float* final_state, void* workspace, size_t workspace_bytes,
                      void* stream);
+
+/* Prefill with the B / C normalisation and biases of the Mamba-3 block fused
+ * into the prologue (Mamba-3 summary page, §3.4: an RMS normalisation of the B
+ * and C projections, then a learnable bias per head and per channel, then the
+ * data-dependent rotation).  The pages fix neither the norm's scale nor its
+ * epsilon; this entry point takes a scale per channel shared by the heads and
+ * ranks and a bias per head and channel shared by the ranks:
+ *   B^[b,t,h,r,n] = B[b,t,h,r,n] / sqrt(mean_n' B[b,t,h,r,n']^2 + eps) * norm_B[n]
+ *                   + bias_B[h,n]             (C likewise with norm_C, bias_C)
+ * and runs the scan of m3_scan_fwd on the raw B, C with B^, C^ in their place
+ * (normalised, biased and rotated in fp32, rounded to bf16 once).
+ *   norm_B, norm_C [N]     fp32   bias_B, bias_C [h, N] fp32   (all required)
+ *   eps                    finite, >= 0 (M3_ERR_VALUE otherwise)
+ * Every other argument as in m3_scan_fwd.  Only the tensor-core kernel's shapes
+ * take it (bf16, P = 64, N in {64, 128}, R in {1, 2, 4}); other shapes return
+ * M3_ERR_UNSUPPORTED.  The decode step takes B_t, C_t already normalised (a few
+ * hundred bytes per token next to the state).  T == 0 writes only final_state
+ * (zero). */
+M3_API int m3_scan_fwd_bcnorm(const m3_dims* d, const void* x, const float* dt, const float* A,
+                       const void* B, const void* C, const float* lambda, const void* theta,
+                       const float* norm_B, const float* norm_C, const float* bias_B,
+                       const float* bias_C, float eps, void* y, float* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* One decode step for every (b, h) (same recurrence, one token):
  *   state   [b, h, N, P]  fp32, read and overwritten with h'_t (complex frame)

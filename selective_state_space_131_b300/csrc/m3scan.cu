@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 
 #include "m3scan.h"
@@ -234,6 +235,38 @@ int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const float* A
                             workspace_bytes, stream);
 }
 
+int m3_scan_fwd_bcnorm(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B,
+                       const void* C, const float* lambda, const void* theta, const float* norm_B, const float* norm_C,
+                       const float* bias_B, const float* bias_C, float eps, void* y, float* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_dims(d, true);
+    if (rc != M3_OK) return rc;
+    (void)workspace;
+    (void)workspace_bytes;
+    const bool has_tokens = d->batch > 0 && d->seqlen > 0;
+    if (has_tokens && (!x || !dt || !A || !B || !C || !y)) return M3_ERR_NULL;
+    if (!norm_B || !norm_C || !bias_B || !bias_C) return M3_ERR_NULL;
+    if (!(eps >= 0.0f) || eps == INFINITY) return M3_ERR_VALUE;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x, B, C, theta, y};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt, A, lambda, norm_B, norm_C, bias_B, bias_C};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (final_state && !aligned16(final_state)) return M3_ERR_ALIGN;
+    if (scan_algorithm(d) != M3_ALGO_CHUNKED_TC) return M3_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d->batch == 0) return M3_OK;
+    if (d->seqlen == 0) {
+        if (!final_state) return M3_OK;
+        const size_t state_bytes = sizeof(float) * d->batch * d->heads * d->dstate * d->headdim;
+        return cudaMemsetAsync(final_state, 0, state_bytes, s) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+    }
+    return m3ws::launch(*d, x, dt, A, B, C, lambda, theta, nullptr, nullptr, nullptr, y, final_state, s, norm_B, norm_C,
+                        bias_B, bias_C, eps);
+}
+
 int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A, const void* B_t,
             const void* C_t, const float* lambda_t, const void* theta_t, const void* prev_B, const void* prev_x,
             void* y_t, void* stream) {
@@ -297,6 +330,7 @@ const char* m3_status_string(int status) {
         case M3_ERR_UNSUPPORTED: return "no kernel for these sizes";
         case M3_ERR_DEVICE: return "a kernel reported a device-side error";
         case M3_ERR_WORKSPACE: return "workspace too small";
+        case M3_ERR_VALUE: return "a scalar argument is out of range";
     }
     return "unknown status";
 }

@@ -71,7 +71,7 @@ constexpr uint32_t kDescHi = ptx::sdesc_hi(1024, ptx::kSwz128);
 __host__ __device__ constexpr int align1k(int x) { return (x + 1023) & ~1023; }
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 
-template <int NSLAB, int R, bool ROT>
+template <int NSLAB, int R, bool ROT, bool NORM = false>
 struct Cfg {
     static constexpr int Q = kRows / R;          // tokens per chunk
     static constexpr int N = 64 * NSLAB;         // state size
@@ -105,7 +105,9 @@ struct Cfg {
     // dt and lambda of a chunk's Q tokens and the token after it, per stage: float [2][2][DL]
     static constexpr int DL = (Q + 1 + 3) & ~3;
     static constexpr int OFF_DL = OFF_CARRY + 2 * K * 4;
-    static constexpr int SMEM_BYTES = OFF_DL + 2 * 2 * DL * 4 + 1024;  // + alignment slack
+    // with the B / C normalisation: its scales and this head's biases, float [4][N]
+    static constexpr int OFF_NRM = OFF_DL + 2 * 2 * DL * 4;
+    static constexpr int SMEM_BYTES = OFF_NRM + (NORM ? 4 * N * 4 : 0) + 1024;  // + alignment slack
     // theta tile [Q][K] as the MN-major B operand of Phi = L theta: 64-byte
     // swizzle for K = 32 pairs, 128-byte swizzle for K = 64
     static constexpr uint32_t TH_SBO = (K == 32) ? 512 : 1024;
@@ -130,6 +132,12 @@ struct Params {
     const float* h0;
     const __nv_bfloat16* prev_B;
     const __nv_bfloat16* prev_x;
+    // B / C normalisation (all null without it): scales [N], biases [h, N], epsilon
+    const float* norm_wB;
+    const float* norm_wC;
+    const float* norm_bB;
+    const float* norm_bC;
+    float norm_eps;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -174,12 +182,12 @@ __device__ __forceinline__ uint32_t swz(int row, int g) {
     return (uint32_t)(row * 128 + (((g & 7) ^ (row & 7)) << 4) + (g >> 3) * (kRows * 128));
 }
 
-template <int NSLAB, int R, bool ROT>
+template <int NSLAB, int R, bool ROT, bool NORM>
 __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     m3_scan_ws_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_B,
                       const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_th,
                       const __grid_constant__ CUtensorMap map_y, const Params prm) {
-    using CF = Cfg<NSLAB, R, ROT>;
+    using CF = Cfg<NSLAB, R, ROT, NORM>;
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -225,6 +233,15 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         ptx::tmem_relinquish();
     }
     if (tid < 2 * K) s_carry[tid] = 0.0f;
+    if constexpr (NORM) {
+        float* nrm = reinterpret_cast<float*>(smem + CF::OFF_NRM);   // wB | wC | bB[h] | bC[h]
+        for (int i = tid; i < N; i += kThreads) {
+            nrm[i] = __ldg(prm.norm_wB + i);
+            nrm[N + i] = __ldg(prm.norm_wC + i);
+            nrm[2 * N + i] = __ldg(prm.norm_bB + (int64_t)h * N + i);
+            nrm[3 * N + i] = __ldg(prm.norm_bC + (int64_t)h * N + i);
+        }
+    }
     // fp32 chunk state G, rows owned by the consumer threads (M = 64 accumulator
     // layout for N = 64: row 16 w + lane % 16, columns 32 (lane / 16) + [0, 32);
     // M = 128 layout for N = 128: row 32 w + lane, all 64 columns)
@@ -489,7 +506,53 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 uint4 vb[GPT];
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) vb[g] = *reinterpret_cast<const uint4*>(sb + swz(row, hf * GPT + g));
-                if (ROT) {
+                if constexpr (NORM) {
+                    // B / C normalisation of the Mamba-3 block (§3.4): each row (one token
+                    // and rank) is divided by its RMS over N, scaled and given this head's
+                    // bias, in fp32; with theta it is then rotated, and rounded to bf16 once.
+                    // The two halves of a row sit in lanes l and l ^ 16.  B first (vb is
+                    // kept for B~'), then C; one 16-byte group at a time, its scales and
+                    // biases read just before use.
+                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);
+                    auto norm_rows = [&](uint4 (&v)[GPT], const float* w, const float* bias, uint8_t* dst) {
+                        float ss = 0.0f;
+#pragma unroll
+                        for (int g = 0; g < GPT; ++g) {
+                            const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v[g]);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pv[m]), bf_lo(pv[m]), fmaf(bf_hi(pv[m]), bf_hi(pv[m]), ss));
+                        }
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                        const float inv = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
+#pragma unroll
+                        for (int g = 0; g < GPT; ++g) {
+                            uint32_t* pv = reinterpret_cast<uint32_t*>(&v[g]);
+                            const int n0 = (hf * GPT + g) * 8;   // the group's first column
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 wv = *reinterpret_cast<const float2*>(w + n0 + 2 * m);
+                                const float2 bv = *reinterpret_cast<const float2*>(bias + n0 + 2 * m);
+                                float a = fmaf(bf_lo(pv[m]) * inv, wv.x, bv.x), b = fmaf(bf_hi(pv[m]) * inv, wv.y, bv.y);
+                                if (ROT) {
+                                    // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
+                                    const float co = cn[g * 4 + m], si = sn[g * 4 + m];
+                                    const float t = a;
+                                    a = fmaf(t, co, b * si);
+                                    b = fmaf(b, co, -t * si);
+                                }
+                                pv[m] = pack_bf16(a, b);
+                            }
+                            *reinterpret_cast<uint4*>(dst + swz(row, hf * GPT + g)) = v[g];
+                            asm volatile("" ::: "memory");   // the next group's loads stay behind
+                        }
+                    };
+                    norm_rows(vb, nrm, nrm + 2 * N, sb);
+                    if (ROT && !fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
+                    uint4 vc[GPT];
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
+                    norm_rows(vc, nrm + N, nrm + 3 * N, scc);
+                } else if (ROT) {
                     if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
                     uint4 vc[GPT];
 #pragma unroll
@@ -889,10 +952,10 @@ inline bool make_map_theta(CUtensorMap* m, const void* base, const m3_dims& d, i
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NSLAB, int R, bool ROT>
+template <int NSLAB, int R, bool ROT, bool NORM>
 int launch_cfg(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cudaStream_t s) {
-    using CF = Cfg<NSLAB, R, ROT>;
-    auto k = m3_scan_ws_kernel<NSLAB, R, ROT>;
+    using CF = Cfg<NSLAB, R, ROT, NORM>;
+    auto k = m3_scan_ws_kernel<NSLAB, R, ROT, NORM>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return M3_ERR_CUDA;
     k<<<(unsigned)(d.batch * d.heads), kThreads, CF::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
@@ -900,19 +963,26 @@ int launch_cfg(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cud
     return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
-template <int NSLAB, bool ROT>
+template <int NSLAB, bool ROT, bool NORM>
 int launch_r(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cudaStream_t s) {
     switch (d.rank) {
-        case 1: return launch_cfg<NSLAB, 1, ROT>(d, maps, prm, s);
-        case 2: return launch_cfg<NSLAB, 2, ROT>(d, maps, prm, s);
-        case 4: return launch_cfg<NSLAB, 4, ROT>(d, maps, prm, s);
+        case 1: return launch_cfg<NSLAB, 1, ROT, NORM>(d, maps, prm, s);
+        case 2: return launch_cfg<NSLAB, 2, ROT, NORM>(d, maps, prm, s);
+        case 4: return launch_cfg<NSLAB, 4, ROT, NORM>(d, maps, prm, s);
     }
     return M3_ERR_UNSUPPORTED;
 }
 
+template <int NSLAB, bool NORM>
+int launch_n(const m3_dims& d, const CUtensorMap* maps, const Params& prm, bool rot, cudaStream_t s) {
+    return rot ? launch_r<NSLAB, true, NORM>(d, maps, prm, s) : launch_r<NSLAB, false, NORM>(d, maps, prm, s);
+}
+
 inline int launch(const m3_dims& d, const void* x, const float* dt, const float* A, const void* B, const void* C,
                   const float* lam, const void* theta, const float* h0, const void* prev_B, const void* prev_x,
-                  void* y, float* final_state, cudaStream_t s) {
+                  void* y, float* final_state, cudaStream_t s, const float* norm_wB = nullptr,
+                  const float* norm_wC = nullptr, const float* norm_bB = nullptr, const float* norm_bC = nullptr,
+                  float norm_eps = 0.0f) {
     if (!supports(d)) return M3_ERR_UNSUPPORTED;
     const void* tma_ptrs[] = {x, B, C, theta, y};
     for (const void* p : tma_ptrs)
@@ -938,8 +1008,15 @@ inline int launch(const m3_dims& d, const void* x, const float* dt, const float*
     prm.h0 = h0;
     prm.prev_B = static_cast<const __nv_bfloat16*>(prev_B);
     prm.prev_x = static_cast<const __nv_bfloat16*>(prev_x);
-    if (d.dstate == 64) return rot ? launch_r<1, true>(d, maps, prm, s) : launch_r<1, false>(d, maps, prm, s);
-    return rot ? launch_r<2, true>(d, maps, prm, s) : launch_r<2, false>(d, maps, prm, s);
+    prm.norm_wB = norm_wB;
+    prm.norm_wC = norm_wC;
+    prm.norm_bB = norm_bB;
+    prm.norm_bC = norm_bC;
+    prm.norm_eps = norm_eps;
+    const bool norm = norm_wB != nullptr;
+    if (d.dstate == 64)
+        return norm ? launch_n<1, true>(d, maps, prm, rot, s) : launch_n<1, false>(d, maps, prm, rot, s);
+    return norm ? launch_n<2, true>(d, maps, prm, rot, s) : launch_n<2, false>(d, maps, prm, rot, s);
 }
 
 }  // namespace m3ws

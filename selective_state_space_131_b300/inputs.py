@@ -124,3 +124,14 @@ def make_decode_inputs(shape: DecodeShape, seed: int, device="cpu"):
         "B": B.to(dt_).contiguous(), "C": C.to(dt_).contiguous(), "lam": lam.contiguous(),
         "theta": theta.to(dt_).contiguous(), "state0": state0.contiguous(),
     }
+
+
+def make_bcnorm_params(dstate: int, heads: int, seed: int, device="cpu"):
+    """Parameters of the B / C normalisation: per-channel scales norm_B, norm_C
+    [N] ~ 1 + 0.1 N(0, 1) and per-head, per-channel biases bias_B, bias_C [h, N]
+    ~ 0.1 N(0, 1), all fp32 (the scales of a trained norm stay near 1)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    n = lambda *shape: torch.randn(*shape, device=device, generator=g)
+    return {"norm_B": 1.0 + 0.1 * n(dstate), "norm_C": 1.0 + 0.1 * n(dstate),
+            "bias_B": 0.1 * n(heads, dstate), "bias_C": 0.1 * n(heads, dstate)}

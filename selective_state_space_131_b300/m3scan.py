@@ -24,6 +24,7 @@ M3_F32, M3_BF16 = 0, 1
 M3_OK = 0
 M3_ERR_NULL, M3_ERR_SHAPE, M3_ERR_DTYPE, M3_ERR_ALIGN = -1, -2, -3, -4
 M3_ERR_CUDA, M3_ERR_UNSUPPORTED, M3_ERR_DEVICE, M3_ERR_WORKSPACE = -5, -6, -7, -8
+M3_ERR_VALUE = -9
 M3_ALGO_NONE, M3_ALGO_SEQUENTIAL, M3_ALGO_CHUNKED_TC = -1, 0, 1
 
 
@@ -43,6 +44,8 @@ _lib.m3_scan_fwd.argtypes = [_dp] + [_vp] * 10 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_fwd.restype = ctypes.c_int
 _lib.m3_scan_fwd_from.argtypes = [_dp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_fwd_from.restype = ctypes.c_int
+_lib.m3_scan_fwd_bcnorm.argtypes = [_dp] + [_vp] * 11 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_size_t, _vp]
+_lib.m3_scan_fwd_bcnorm.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
 _lib.m3_device_status.argtypes = [_vp]
@@ -138,6 +141,30 @@ def m3_scan_fwd_from(x, dt, A, B, C, lam, theta, initial_state, prev_B, prev_x, 
                                _ptr(final_state), _ptr(workspace), int(workspace_bytes), _stream(stream))
     if rc != M3_OK:
         raise M3Error(rc, "m3_scan_fwd_from")
+
+
+def m3_scan_fwd_bcnorm(x, dt, A, B, C, lam, theta, norm_B, norm_C, bias_B, bias_C, eps: float, y, final_state,
+                       chunk: int = 64, workspace=None, workspace_bytes: int = 0, stream=None,
+                       dims: m3_dims | None = None) -> None:
+    """Prefill with the B / C normalisation and biases fused into the prologue:
+    norm_B / norm_C [N] fp32 scales, bias_B / bias_C [h, N] fp32 biases, eps >= 0.
+    Raises M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, chunk)
+    rc = _lib.m3_scan_fwd_bcnorm(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam),
+                                 _ptr(theta), _ptr(norm_B), _ptr(norm_C), _ptr(bias_B), _ptr(bias_C), float(eps),
+                                 _ptr(y), _ptr(final_state), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_scan_fwd_bcnorm")
+
+
+def raw_scan_fwd_bcnorm(dims: m3_dims, ptrs, eps: float, stream=None) -> int:
+    """Direct call with raw addresses (x, dt, A, B, C, lam, theta, norm_B, norm_C,
+    bias_B, bias_C, y, final_state, workspace, workspace_bytes) and eps; returns
+    the status code."""
+    *p, ws_bytes = ptrs
+    return int(_lib.m3_scan_fwd_bcnorm(ctypes.byref(dims), *p[:11], ctypes.c_float(eps), *p[11:], int(ws_bytes),
+                                       stream))
 
 
 def m3_step(state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, stream=None,

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(m3):
 
 
 def test_status_strings(m3):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert m3.m3_status_string(code) != "unknown status"
     assert m3.m3_status_string(-99) == "unknown status"
 
@@ -123,3 +123,24 @@ def test_scan_from_validation(m3):
     assert m3.raw_scan_fwd_from(_dims(m3), _from_ptrs(pB=FAKE + 1)) == m3.M3_ERR_ALIGN
     assert m3.raw_scan_fwd_from(_dims(m3, dstate=7), _from_ptrs()) == m3.M3_ERR_SHAPE
     assert m3.raw_scan_fwd_from(_dims(m3, batch=0), _from_ptrs(x=None, y=None)) == m3.M3_OK
+
+
+def _bcnorm_ptrs(**over):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, lam=FAKE, theta=FAKE, wB=FAKE, wC=FAKE, bB=FAKE, bC=FAKE,
+             y=FAKE, fs=FAKE, ws=None, wsb=0)
+    p.update(over)
+    return [p[k] for k in ("x", "dt", "A", "B", "C", "lam", "theta", "wB", "wC", "bB", "bC", "y", "fs", "ws", "wsb")]
+
+
+def test_scan_bcnorm_validation(m3):
+    d = _dims(m3)
+    for k in ("wB", "wC", "bB", "bC"):
+        assert m3.raw_scan_fwd_bcnorm(d, _bcnorm_ptrs(**{k: None}), 1e-6) == m3.M3_ERR_NULL
+        assert m3.raw_scan_fwd_bcnorm(d, _bcnorm_ptrs(**{k: FAKE + 2}), 1e-6) == m3.M3_ERR_ALIGN
+    for eps in (-1e-6, float("inf"), float("nan")):
+        assert m3.raw_scan_fwd_bcnorm(d, _bcnorm_ptrs(), eps) == m3.M3_ERR_VALUE
+    # only the tensor-core kernel's shapes take the fused normalisation
+    assert m3.raw_scan_fwd_bcnorm(_dims(m3, dtype=m3.M3_F32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
+    assert m3.raw_scan_fwd_bcnorm(_dims(m3, headdim=32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
+    assert m3.raw_scan_fwd_bcnorm(_dims(m3, dstate=7), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd_bcnorm(_dims(m3, batch=0), _bcnorm_ptrs(x=None, y=None), 1e-6) == m3.M3_OK
