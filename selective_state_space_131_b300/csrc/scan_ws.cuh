@@ -234,12 +234,24 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     }
     if (tid < 2 * K) s_carry[tid] = 0.0f;
     if constexpr (NORM) {
-        float* nrm = reinterpret_cast<float*>(smem + CF::OFF_NRM);   // wB | wC | bB[h] | bC[h]
+        // the scales and this head's biases: with the rotation wB | wC | bB | bC
+        // (float [4][N]); without it B and C interleaved per channel, (wB[n], wC[n])
+        // at 2 n and (bB[n], bC[n]) at 2 N + 2 n
+        float* nrm = reinterpret_cast<float*>(smem + CF::OFF_NRM);
         for (int i = tid; i < N; i += kThreads) {
-            nrm[i] = __ldg(prm.norm_wB + i);
-            nrm[N + i] = __ldg(prm.norm_wC + i);
-            nrm[2 * N + i] = __ldg(prm.norm_bB + (int64_t)h * N + i);
-            nrm[3 * N + i] = __ldg(prm.norm_bC + (int64_t)h * N + i);
+            const float v[4] = {__ldg(prm.norm_wB + i), __ldg(prm.norm_wC + i), __ldg(prm.norm_bB + (int64_t)h * N + i),
+                                __ldg(prm.norm_bC + (int64_t)h * N + i)};
+            if (ROT) {
+                nrm[i] = v[0];
+                nrm[N + i] = v[1];
+                nrm[2 * N + i] = v[2];
+                nrm[3 * N + i] = v[3];
+            } else {
+                nrm[2 * i] = v[0];
+                nrm[2 * i + 1] = v[1];
+                nrm[2 * N + 2 * i] = v[2];
+                nrm[2 * N + 2 * i + 1] = v[3];
+            }
         }
     }
     // fp32 chunk state G, rows owned by the consumer threads (M = 64 accumulator
@@ -506,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 uint4 vb[GPT];
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) vb[g] = *reinterpret_cast<const uint4*>(sb + swz(row, hf * GPT + g));
-                if constexpr (NORM) {
+                if constexpr (NORM && ROT) {
                     // B / C normalisation of the Mamba-3 block (§3.4): each row (one token
                     // and rank) is divided by its RMS over N, scaled and given this head's
                     // bias, in fp32; with theta it is then rotated, and rounded to bf16 once.
@@ -552,6 +564,57 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
                     norm_rows(vc, nrm + N, nrm + 3 * N, scc);
+                } else if constexpr (NORM) {
+                    // the same normalisation without a rotation: B and C together in packed
+                    // fp32x2 math, u = (a_B, a_C), v = (b_B, b_C) for a pair's elements (a, b)
+                    // (without theta every tile of the chunk is already in)
+                    uint4 vc[GPT];
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
+                    float2 ss = make_float2(0.0f, 0.0f);   // (B row, C row) sums of squares
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        const uint32_t* pb = reinterpret_cast<const uint32_t*>(&vb[g]);
+                        const uint32_t* pc = reinterpret_cast<const uint32_t*>(&vc[g]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 u = make_float2(bf_lo(pb[m]), bf_lo(pc[m]));
+                            const float2 v = make_float2(bf_hi(pb[m]), bf_hi(pc[m]));
+                            ss = __ffma2_rn(u, u, __ffma2_rn(v, v, ss));
+                        }
+                    }
+                    // the tiles are unpacked again below rather than kept as 64 fp32 values
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        asm volatile("" : "+r"(vb[g].x), "+r"(vb[g].y), "+r"(vb[g].z), "+r"(vb[g].w));
+                        asm volatile("" : "+r"(vc[g].x), "+r"(vc[g].y), "+r"(vc[g].z), "+r"(vc[g].w));
+                    }
+                    ss.x += __shfl_xor_sync(0xffffffffu, ss.x, 16);
+                    ss.y += __shfl_xor_sync(0xffffffffu, ss.y, 16);
+                    const float2 inv = make_float2(rsqrtf(fmaf(ss.x, 1.0f / N, prm.norm_eps)),
+                                                   rsqrtf(fmaf(ss.y, 1.0f / N, prm.norm_eps)));
+                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        uint32_t* pb = reinterpret_cast<uint32_t*>(&vb[g]);
+                        uint32_t* pc = reinterpret_cast<uint32_t*>(&vc[g]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int n = (hf * GPT + g) * 8 + 2 * m;   // column of the pair's first element
+                            const float4 w = *reinterpret_cast<const float4*>(nrm + 2 * n);           // wB, wC at n, n + 1
+                            const float4 bi = *reinterpret_cast<const float4*>(nrm + 2 * N + 2 * n);  // biases likewise
+                            const float2 u = __ffma2_rn(__fmul2_rn(make_float2(bf_lo(pb[m]), bf_lo(pc[m])), inv),
+                                                        make_float2(w.x, w.y), make_float2(bi.x, bi.y));
+                            const float2 v = __ffma2_rn(__fmul2_rn(make_float2(bf_hi(pb[m]), bf_hi(pc[m])), inv),
+                                                        make_float2(w.z, w.w), make_float2(bi.z, bi.w));
+                            pb[m] = pack_bf16(u.x, v.x);
+                            pc[m] = pack_bf16(u.y, v.y);
+                        }
+                        const uint32_t off = swz(row, hf * GPT + g);
+                        *reinterpret_cast<uint4*>(sb + off) = vb[g];
+                        *reinterpret_cast<uint4*>(scc + off) = vc[g];
+                        asm volatile("" ::: "memory");   // the next group's scale / bias loads stay behind
+                    }
                 } else if (ROT) {
                     if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
                     uint4 vc[GPT];
