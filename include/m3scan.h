@@ -1,7 +1,8 @@
 /*
  * m3scan.h -- C ABI of libm3scan.so, the B300 (sm_103a) Mamba-3 selective
- * SSM scan: a chunked prefill (m3_scan_fwd) and a single-token decode step
- * (m3_step).
+ * SSM scan: a chunked prefill (m3_scan_fwd; m3_scan_fwd_from continues a
+ * sequence from a state; m3_scan_fwd_bcnorm fuses the block's B / C
+ * normalisation) and a single-token decode step (m3_step).
  *
  * The operation (Mamba-3 summary page, "Mamba-3: Expressive SSM with MIMO"):
  * for every batch row b and head h independently, with scalar A_h < 0 and

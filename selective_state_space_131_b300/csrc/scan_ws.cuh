@@ -27,12 +27,16 @@
 // overflow; only the diagonal block needs one exp per element.
 //
 // Roles (256 threads, one CTA per (b, h), two CTAs per SM when N = 64):
-//   warpgroup 0 (threads 0-127), chunk c+1: scalars (cs, gamma, w, scales),
-//     cumulative angles, rotation of B and C in shared memory, the scaled copy
-//     B~'; then thread 0 issues S and dG.
-//   warpgroup 1 (threads 128-255), chunk c: mask S -> S', issue Y_inter and
-//     Y_intra, G update, y epilogue + TMA store; thread 128 also issues every
-//     TMA load (two stages ahead of warpgroup 0).
+//   warpgroup 0 (threads 0-127), chunk c+1: scalars (warp 0, from dt / lambda it
+//     copied into shared memory one chunk ahead), cumulative angles, rotation of
+//     B and C in shared memory (with the fused B / C normalisation first, in the
+//     NORM variants), the scaled copy B~'.  Lane 0 of warp 1 issues Phi and
+//     Y_inter, lane 0 of warp 2 issues S and dG.
+//   warpgroup 1 (threads 128-255), chunk c: mask S -> S', G update, y epilogue;
+//     thread 128 issues the TMA store of y, lane 0 of warp 5 issues Y_intra and
+//     lane 0 of warp 6 every TMA load: two stages, each filled in two parts when
+//     the rotation is on (theta + B as soon as S has read them, C + x after
+//     Y_intra), in one part otherwise.
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // word, the decision to stop is voted at the next named barrier (uniform in the
 // warpgroup), and the CTA waits (bounded) for its copies and MMAs in flight and
