@@ -182,6 +182,16 @@ M3_API int m3_step(const m3_dims* d, float* state, const void* x_t, const float*
  * device-side error since the last call, or M3_ERR_CUDA. */
 M3_API int m3_device_status(void* stream);
 
+/* Self-test of the failure detection (no counterpart on the pages): launches
+ * one CTA whose first thread waits, with a budget of budget_cycles clock
+ * cycles, on an mbarrier that nothing completes -- the bounded wait every
+ * kernel of this library uses.  When the budget runs out the thread records a
+ * wait timeout in the device status word and the kernel returns, leaving the
+ * context usable; m3_device_status() then returns M3_ERR_DEVICE and clears it.
+ *   budget_cycles  in [1, 4e9] (M3_ERR_VALUE otherwise)
+ * Returns M3_OK once the launch is enqueued, or M3_ERR_CUDA. */
+M3_API int m3_selftest_wait_timeout(long long budget_cycles, void* stream);
+
 /* Static text for a status code. */
 M3_API const char* m3_status_string(int status);
 

@@ -12,6 +12,7 @@
 #include "step_simt.cuh"
 #include "step_fast.cuh"
 #include "scan_ws.cuh"
+#include "selftest.cuh"
 
 namespace {
 
@@ -317,6 +318,12 @@ int m3_device_status(void* stream) {
         return M3_ERR_DEVICE;
     }
     return M3_OK;
+}
+
+int m3_selftest_wait_timeout(long long budget_cycles, void* stream) {
+    if (budget_cycles < 1 || budget_cycles > 4000000000LL) return M3_ERR_VALUE;
+    m3::m3_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(budget_cycles);
+    return launch_status();
 }
 
 const char* m3_status_string(int status) {

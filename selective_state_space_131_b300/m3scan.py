@@ -48,6 +48,8 @@ _lib.m3_scan_fwd_bcnorm.argtypes = [_dp] + [_vp] * 11 + [ctypes.c_float] + [_vp]
 _lib.m3_scan_fwd_bcnorm.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
+_lib.m3_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _vp]
+_lib.m3_selftest_wait_timeout.restype = ctypes.c_int
 _lib.m3_device_status.argtypes = [_vp]
 _lib.m3_device_status.restype = ctypes.c_int
 _lib.m3_status_string.argtypes = [ctypes.c_int]
@@ -176,6 +178,13 @@ def m3_step(state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, 
                       _ptr(lam_t), _ptr(theta_t), _ptr(prev_B), _ptr(prev_x), _ptr(y_t), _stream(stream))
     if rc != M3_OK:
         raise M3Error(rc, "m3_step")
+
+
+def m3_selftest_wait_timeout(budget_cycles: int, stream=None) -> int:
+    """Launch the bounded-wait self-test (a wait that nothing satisfies, given
+    up after budget_cycles); returns the launch status.  The device status word
+    then reports the timeout through m3_device_status()."""
+    return int(_lib.m3_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
 def m3_device_status(stream=None) -> int:

@@ -144,3 +144,9 @@ def test_scan_bcnorm_validation(m3):
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, headdim=32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, dstate=7), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_SHAPE
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, batch=0), _bcnorm_ptrs(x=None, y=None), 1e-6) == m3.M3_OK
+
+
+def test_selftest_wait_timeout_validation(m3):
+    assert m3.m3_selftest_wait_timeout(0, 0) == m3.M3_ERR_VALUE
+    assert m3.m3_selftest_wait_timeout(-5, 0) == m3.M3_ERR_VALUE
+    assert m3.m3_selftest_wait_timeout(5_000_000_000, 0) == m3.M3_ERR_VALUE
