@@ -73,6 +73,9 @@ def _ptr(t):
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        # the C ABI takes C-contiguous buffers; a strided view would be read as one
+        raise ValueError(f"tensor of shape {tuple(t.shape)} is not contiguous; pass .contiguous()")
     return t.data_ptr()
 
 
