@@ -150,3 +150,13 @@ def test_selftest_wait_timeout_validation(m3):
     assert m3.m3_selftest_wait_timeout(0, 0) == m3.M3_ERR_VALUE
     assert m3.m3_selftest_wait_timeout(-5, 0) == m3.M3_ERR_VALUE
     assert m3.m3_selftest_wait_timeout(5_000_000_000, 0) == m3.M3_ERR_VALUE
+
+
+def test_binding_rejects_strided_tensors(m3):
+    import torch
+    t = torch.zeros(4, 6)
+    assert m3._ptr(t) == t.data_ptr()
+    with pytest.raises(ValueError):
+        m3._ptr(t.t())                  # a transposed view is not C-contiguous
+    with pytest.raises(ValueError):
+        m3._ptr(torch.zeros(3, 5, 2)[:, 1])
