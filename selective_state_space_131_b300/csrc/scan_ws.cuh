@@ -483,6 +483,39 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 
             // (2) this chunk's tiles; the angles of this thread's row and pairs
             bool fail = !ptx::mbar_wait(&bar_lda[s], (c >> 1) & 1, kWaitBudget);
+            if constexpr (NORM && ROT) {
+                // B / C normalisation of the Mamba-3 block (§3.4), B's part: each row
+                // (one token and rank) divided by its RMS over N, scaled and given this
+                // head's bias in fp32 and rounded to bf16 in place, before the angles
+                // (no sine or cosine is live yet).  The two halves of a row sit in lanes
+                // l and l ^ 16.
+                const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);   // wB | wC | bB | bC
+                uint8_t* sbn = st + CF::ST_B;
+                uint4 v[GPT];
+#pragma unroll
+                for (int g = 0; g < GPT; ++g) v[g] = *reinterpret_cast<const uint4*>(sbn + swz(row, hf * GPT + g));
+                float ss = 0.0f;
+#pragma unroll
+                for (int g = 0; g < GPT; ++g) {
+                    const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v[g]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pv[m]), bf_lo(pv[m]), fmaf(bf_hi(pv[m]), bf_hi(pv[m]), ss));
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                const float inv = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
+#pragma unroll
+                for (int g = 0; g < GPT; ++g) {
+                    uint32_t* pv = reinterpret_cast<uint32_t*>(&v[g]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int n = (hf * GPT + g) * 8 + 2 * m;   // column of the pair's first element
+                        const float2 w = *reinterpret_cast<const float2*>(nrm + n);
+                        const float2 bi = *reinterpret_cast<const float2*>(nrm + 2 * N + n);
+                        pv[m] = pack_bf16(fmaf(bf_lo(pv[m]) * inv, w.x, bi.x), fmaf(bf_hi(pv[m]) * inv, w.y, bi.y));
+                    }
+                    *reinterpret_cast<uint4*>(sbn + swz(row, hf * GPT + g)) = v[g];
+                }
+            }
             float cn[PH], sn[PH];
             if (ROT) {
                 if (!fail) fail = !ptx::mbar_wait(&bar_phi, c & 1, kWaitBudget);
@@ -523,51 +556,46 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) vb[g] = *reinterpret_cast<const uint4*>(sb + swz(row, hf * GPT + g));
                 if constexpr (NORM && ROT) {
-                    // B / C normalisation of the Mamba-3 block (§3.4): each row (one token
-                    // and rank) is divided by its RMS over N, scaled and given this head's
-                    // bias, in fp32; with theta it is then rotated, and rounded to bf16 once.
-                    // The two halves of a row sit in lanes l and l ^ 16.  B first (vb is
-                    // kept for B~'), then C; one 16-byte group at a time, its scales and
-                    // biases read just before use.
-                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);
-                    auto norm_rows = [&](uint4 (&v)[GPT], const float* w, const float* bias, uint8_t* dst) {
-                        float ss = 0.0f;
+                    // C's normalisation (B's ran in step (2)), then the joint rotation of
+                    // the plain path: C's row sum of squares over one 16-byte group at a
+                    // time, then per group normalise C, rotate B and C, store both
+                    if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
+                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);   // wB | wC | bB | bC
+                    float ss = 0.0f;
 #pragma unroll
-                        for (int g = 0; g < GPT; ++g) {
-                            const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v[g]);
+                    for (int g = 0; g < GPT; ++g) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
+                        const uint32_t pq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pv[m]), bf_lo(pv[m]), fmaf(bf_hi(pv[m]), bf_hi(pv[m]), ss));
+                        for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pq[m]), bf_lo(pq[m]), fmaf(bf_hi(pq[m]), bf_hi(pq[m]), ss));
+                    }
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                    const float ic = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        const uint32_t off = swz(row, hf * GPT + g);
+                        uint4 q = *reinterpret_cast<const uint4*>(scc + off);
+                        uint32_t* pb = reinterpret_cast<uint32_t*>(&vb[g]);
+                        uint32_t* pc = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int n = (hf * GPT + g) * 8 + 2 * m;
+                            const float2 w = *reinterpret_cast<const float2*>(nrm + N + n);
+                            const float2 bi = *reinterpret_cast<const float2*>(nrm + 3 * N + n);
+                            // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos), for the B pair
+                            // and the normalised C pair at once: u = (a_B, a_C), v = (b_B, b_C)
+                            const float2 u = make_float2(bf_lo(pb[m]), fmaf(bf_lo(pc[m]) * ic, w.x, bi.x));
+                            const float2 v = make_float2(bf_hi(pb[m]), fmaf(bf_hi(pc[m]) * ic, w.y, bi.y));
+                            const float co = cn[g * 4 + m], si = sn[g * 4 + m];
+                            const float2 c2 = make_float2(co, co), s2 = make_float2(si, si), ns2 = make_float2(-si, -si);
+                            const float2 u2 = __ffma2_rn(u, c2, __fmul2_rn(v, s2));
+                            const float2 v2 = __ffma2_rn(v, c2, __fmul2_rn(u, ns2));
+                            pb[m] = pack_bf16(u2.x, v2.x);
+                            pc[m] = pack_bf16(u2.y, v2.y);
                         }
-                        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                        const float inv = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
-#pragma unroll
-                        for (int g = 0; g < GPT; ++g) {
-                            uint32_t* pv = reinterpret_cast<uint32_t*>(&v[g]);
-                            const int n0 = (hf * GPT + g) * 8;   // the group's first column
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const float2 wv = *reinterpret_cast<const float2*>(w + n0 + 2 * m);
-                                const float2 bv = *reinterpret_cast<const float2*>(bias + n0 + 2 * m);
-                                float a = fmaf(bf_lo(pv[m]) * inv, wv.x, bv.x), b = fmaf(bf_hi(pv[m]) * inv, wv.y, bv.y);
-                                if (ROT) {
-                                    // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
-                                    const float co = cn[g * 4 + m], si = sn[g * 4 + m];
-                                    const float t = a;
-                                    a = fmaf(t, co, b * si);
-                                    b = fmaf(b, co, -t * si);
-                                }
-                                pv[m] = pack_bf16(a, b);
-                            }
-                            *reinterpret_cast<uint4*>(dst + swz(row, hf * GPT + g)) = v[g];
-                            asm volatile("" ::: "memory");   // the next group's loads stay behind
-                        }
-                    };
-                    norm_rows(vb, nrm, nrm + 2 * N, sb);
-                    if (ROT && !fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
-                    uint4 vc[GPT];
-#pragma unroll
-                    for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
-                    norm_rows(vc, nrm + N, nrm + 3 * N, scc);
+                        *reinterpret_cast<uint4*>(sb + off) = vb[g];
+                        *reinterpret_cast<uint4*>(scc + off) = q;
+                    }
                 } else if constexpr (NORM) {
                     // the same normalisation without a rotation: B and C together in packed
                     // fp32x2 math, u = (a_B, a_C), v = (b_B, b_C) for a pair's elements (a, b)
