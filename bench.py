@@ -42,9 +42,9 @@ HBM_FALLBACK_GBS = 6400.0
 # T = 8192 (traffic grows with the sequence length); the summary with its
 # command is profiles/m3_scan_ws_siso_b8T2048P64N64.md.
 NCU_TRAFFIC = {
-    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.218176e6 + 48.027392e6),
+    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.210240e6 + 48.293120e6),
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
-                                      "sha256": "99e0dce26c5aea7c"},
+                                      "sha256": "bc29f03bb103d091"},
 }
 
 
