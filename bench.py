@@ -39,8 +39,7 @@ HBM_FALLBACK_GBS = 6400.0
 # prefill kernel from one ncu capture, keyed by workload, with the sha256 prefix
 # of the kernel source the counters were taken on: reported only while the
 # source is unchanged, else null.  Captured at T = 2048 and scaled x4 to
-# T = 8192 (traffic grows with the sequence length); the summary with its
-# command is profiles/m3_scan_ws_siso_b8T2048P64N64.md.
+# T = 8192 (traffic grows with the sequence length).
 NCU_TRAFFIC = {
     "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.210240e6 + 48.293120e6),
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
@@ -426,11 +425,13 @@ def main():
 
     if not args.no_e2e:
         # end to end through the public API with host buffers: pinned host -> device
-        # copies of the step's inputs, the prefill, device -> host copy of y.
+        # copies of the step's inputs, the prefill, device -> host copies of its
+        # whole result (y and the final state).
         host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
         y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        fs_host = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-        d2h = y_host.numel() * y_host.element_size()
+        d2h = y_host.numel() * y_host.element_size() + fs_host.numel() * fs_host.element_size()
         e_steps = max(3, min(20, args.steps // 20))
 
         def e2e_step():
@@ -440,6 +441,7 @@ def main():
                         d[k].copy_(v, non_blocking=True)
                 step()
                 y_host.copy_(y, non_blocking=True)
+                fs_host.copy_(fs, non_blocking=True)
         e2e_step()
         torch.cuda.synchronize()
         barrier()

@@ -147,8 +147,11 @@ M3_API int m3_scan_fwd_from(const m3_dims* d, const void* x, const float* dt, co
  * ranks and a bias per head and channel shared by the ranks:
  *   B^[b,t,h,r,n] = B[b,t,h,r,n] / sqrt(mean_n' B[b,t,h,r,n']^2 + eps) * norm_B[n]
  *                   + bias_B[h,n]             (C likewise with norm_C, bias_C)
- * and runs the scan of m3_scan_fwd on the raw B, C with B^, C^ in their place
- * (normalised, biased and rotated in fp32, rounded to bf16 once).
+ * and runs the scan of m3_scan_fwd on the raw B, C with B^, C^ in their place.
+ * The arithmetic is fp32.  With theta, B^ is rounded to bf16 after the
+ * normalisation and again after the rotation, C^ once after its rotation;
+ * without theta each is rounded once.  With eps == 0 an all-zero row of B or C
+ * has no defined normalisation (0 / 0); the kernel maps it to the bias.
  *   norm_B, norm_C [N]     fp32   bias_B, bias_C [h, N] fp32   (all required)
  *   eps                    finite, >= 0 (M3_ERR_VALUE otherwise)
  * Every other argument as in m3_scan_fwd.  Only the tensor-core kernel's shapes

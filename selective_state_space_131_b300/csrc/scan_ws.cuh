@@ -181,6 +181,12 @@ __device__ __forceinline__ float reduce_2pi(float x) {
 __device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
     __sincosf(reduce_2pi(x), s, c);
 }
+// 1 / sqrt(ss / n + eps) of a row's sum of squares ss over n channels, kept
+// finite for an all-zero row (the zero-filled rows past the end of a sequence)
+// when eps is 0: such a row then normalises to 0 instead of 0 * inf = NaN.
+__device__ __forceinline__ float rms_inv(float ss, float inv_n, float eps) {
+    return rsqrtf(fmaxf(fmaf(ss, inv_n, eps), 1.17549435e-38f));
+}
 // Byte offset of the 16-byte group g of row `row` in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int row, int g) {
     return (uint32_t)(row * 128 + (((g & 7) ^ (row & 7)) << 4) + (g >> 3) * (kRows * 128));
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pv[m]), bf_lo(pv[m]), fmaf(bf_hi(pv[m]), bf_hi(pv[m]), ss));
                 }
                 ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                const float inv = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
+                const float inv = rms_inv(ss, 1.0f / N, prm.norm_eps);
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) {
                     uint32_t* pv = reinterpret_cast<uint32_t*>(&v[g]);
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                         for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pq[m]), bf_lo(pq[m]), fmaf(bf_hi(pq[m]), bf_hi(pq[m]), ss));
                     }
                     ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                    const float ic = rsqrtf(fmaf(ss, 1.0f / N, prm.norm_eps));
+                    const float ic = rms_inv(ss, 1.0f / N, prm.norm_eps);
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {
                         const uint32_t off = swz(row, hf * GPT + g);
@@ -623,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     }
                     ss.x += __shfl_xor_sync(0xffffffffu, ss.x, 16);
                     ss.y += __shfl_xor_sync(0xffffffffu, ss.y, 16);
-                    const float2 inv = make_float2(rsqrtf(fmaf(ss.x, 1.0f / N, prm.norm_eps)),
-                                                   rsqrtf(fmaf(ss.y, 1.0f / N, prm.norm_eps)));
+                    const float2 inv = make_float2(rms_inv(ss.x, 1.0f / N, prm.norm_eps),
+                                                   rms_inv(ss.y, 1.0f / N, prm.norm_eps));
                     const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {

@@ -25,7 +25,7 @@ def m3():
     return m3scan
 
 
-def run_and_check(m3, shape, seed, bsel=None, hsel=None):
+def run_and_check(m3, shape, seed, bsel=None, hsel=None, eps=EPS):
     inp = inputs.make_scan_inputs(shape, seed)
     nrm = inputs.make_bcnorm_params(shape.dstate, shape.heads, seed + 1)
     d, nd = dev(inp), dev(nrm)
@@ -33,7 +33,7 @@ def run_and_check(m3, shape, seed, bsel=None, hsel=None):
     y = torch.empty_like(x)
     fs = torch.empty(shape.batch, shape.heads, shape.dstate, shape.headdim, device="cuda")
     m3.m3_scan_fwd_bcnorm(x, d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], nd["norm_B"], nd["norm_C"],
-                          nd["bias_B"], nd["bias_C"], EPS, y, fs, chunk=shape.chunk)
+                          nd["bias_B"], nd["bias_C"], eps, y, fs, chunk=shape.chunk)
     torch.cuda.synchronize()
     assert m3.m3_device_status() == m3.M3_OK
     y, fs = y.float().cpu(), fs.cpu()
@@ -42,8 +42,8 @@ def run_and_check(m3, shape, seed, bsel=None, hsel=None):
         inp = sub_problem(inp, bsel, hsel)
         nrm = {k: (v[hsel] if k.startswith("bias") else v) for k, v in nrm.items()}
     f64 = lambda t: t.double().numpy()   # exact: the bf16 values as fp64
-    Bn = bcnorm(f64(inp["B"]), f64(nrm["norm_B"]), f64(nrm["bias_B"]), EPS)
-    Cn = bcnorm(f64(inp["C"]), f64(nrm["norm_C"]), f64(nrm["bias_C"]), EPS)
+    Bn = bcnorm(f64(inp["B"]), f64(nrm["norm_B"]), f64(nrm["bias_B"]), eps)
+    Cn = bcnorm(f64(inp["C"]), f64(nrm["norm_C"]), f64(nrm["bias_C"]), eps)
     yr, fr = oracle.scan(inp["x"], inp["dt"], inp["A"], Bn, Cn, inp["lam"], inp["theta"])
     ey, ef = max_rel(y, yr), max_rel(fs, fr)
     assert np.isfinite(ey) and np.isfinite(ef)
@@ -75,9 +75,19 @@ def test_bcnorm_small(m3, T, N, R, lam, th):
 
 def test_bcnorm_siso_workload_full_size(m3):
     """The SISO complex + trapezoidal workload (b8 h32 T8192 P64 N64) with the
-    normalisation, on sampled (batch, head) sequences."""
-    ey, ef = run_and_check(m3, inputs.CONFIGS[2], 2, bsel=[0, 7], hsel=[0, 13, 31])
+    normalisation, on 64 sequences: every batch row, eight heads."""
+    ey, ef = run_and_check(m3, inputs.CONFIGS[2], 2, bsel=list(range(8)), hsel=[0, 4, 9, 13, 18, 22, 27, 31])
     print(f"full size: y {ey:.2e} state {ef:.2e}")
+
+
+@pytest.mark.parametrize("T,R,th", [(209, 1, True), (209, 1, False), (130, 4, True)], ids=lambda v: str(v))
+def test_bcnorm_eps_zero_ragged_tail(m3, T, R, th):
+    """eps = 0 with a ragged last chunk: the zero-filled rows past the end of the
+    sequence must not turn into NaN (0 / sqrt(0)) and reach y or the state."""
+    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=64, rank=R, chunk=64 // R,
+                             dtype="bf16", with_theta=th)
+    ey, ef = run_and_check(m3, shape, 3100 + T + R, eps=0.0)
+    print(f"eps 0 T{T} R{R} th{th}: y {ey:.2e} state {ef:.2e}")
 
 
 def test_bcnorm_empty_sequence(m3):

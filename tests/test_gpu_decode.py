@@ -137,3 +137,60 @@ def test_decode_workload_full_size(m3, R):
     shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "rank": R, "steps": 16})
     ey, es = run_chain(m3, shape, 4, 16, sel=([0, 100, 255], [0, 17, 31]))
     assert ey <= 1e-4 and es <= 1e-4, (ey, es)
+
+
+@pytest.mark.parametrize("R", [1, 4])
+def test_decode_sweep_1024_steps_in_graph(m3, R):
+    """The decode sweep the bench times: b256 h32 P64 N64 fp32, 1024 consecutive
+    m3_step calls captured in one CUDA graph.  y and the state are checked
+    against the oracle after every 64th step and at step 1024, on 12 sampled
+    (batch, head) units; the oracle runs the same 1024 tokens in 64-token
+    segments, each started from its own previous segment's final state."""
+    steps, seg = 1024, 64
+    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "rank": R, "steps": steps})
+    inp = inputs.make_decode_inputs(shape, 4 + R, device="cuda")
+    bsel, hsel = [0, 37, 128, 255], [0, 11, 31]
+    state = inp["state0"].clone()
+    ys = torch.empty_like(inp["x"][1:])
+    snaps = torch.empty((steps // seg,) + tuple(state.shape), device="cuda")
+    dims = m3.step_dims(inp["x"][0], inp["B"][0])
+    stream = torch.cuda.Stream()
+
+    def sweep():
+        for s in range(steps):
+            m3.m3_step(state, inp["x"][s + 1], inp["dt"][s + 1], inp["A"], inp["B"][s + 1], inp["C"][s + 1],
+                       inp["lam"][s + 1], inp["theta"][s + 1], inp["B"][s], inp["x"][s], ys[s], stream=stream,
+                       dims=dims)
+            if (s + 1) % seg == 0:
+                snaps[(s + 1) // seg - 1].copy_(state)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        sweep()                                         # uncaptured warm-up, as the bench does
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep()
+    state.copy_(inp["state0"])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    assert m3.m3_device_status() == m3.M3_OK
+
+    sel = lambda a: a[:, bsel][:, :, hsel].cpu()        # [S, b, h, ...] -> sampled units
+    x, dt, B, C, lam, th = (sel(inp[k]) for k in ("x", "dt", "B", "C", "lam", "theta"))
+    A = inp["A"][hsel].cpu()
+    h = inp["state0"][bsel][:, hsel].cpu()
+    yg = ys[:, bsel][:, :, hsel].cpu()                  # [steps, b', h', R, P]
+    sg = snaps[:, bsel][:, :, hsel].cpu()
+    worst = (0.0, 0.0)
+    for k in range(steps // seg):
+        t0, t1 = k * seg + 1, (k + 1) * seg + 1         # tokens of this segment
+        tok = lambda a: a[t0:t1].transpose(0, 1)
+        yr, h = oracle.scan(tok(x), tok(dt), A, tok(B), tok(C), tok(lam), tok(th), h0=h,
+                            prevB=B[t0 - 1], prevx=x[t0 - 1])
+        ey = max_rel(yg[t0 - 1:t1 - 1].transpose(0, 1), yr)
+        es = max_rel(sg[k], h)
+        worst = (max(worst[0], ey), max(worst[1], es))
+        assert ey <= 1e-4 and es <= 1e-4, (k, ey, es)
+    print(f"R{R} 1024 steps: worst segment y {worst[0]:.2e} state {worst[1]:.2e}")
