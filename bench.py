@@ -236,6 +236,69 @@ def run_reference(args, shape, cfg_name):
     }
 
 
+def decode_k_bytes(shape: inputs.DecodeShape, k: int) -> int:
+    """Algorithmic bytes of one k-token decode launch: state read + written
+    once, every token's inputs (x, B, C, theta, dt, lambda) read and y written,
+    the previous token's B and x read once."""
+    b, H, P, N, R = shape.batch, shape.heads, shape.headdim, shape.dstate, shape.rank
+    es = 2 if shape.dtype == "bf16" else 4
+    u = b * H
+    per_tok = R * P * es * 2 + R * N * es * 2 + (N // 2) * es + 8
+    return u * (2 * N * P * 4 + k * per_tok + R * (P + N) * es)
+
+
+def bench_decode_k(m3, stream, steps: int, rank_seed: int, rank: int, k: int):
+    """Multi-token decode of the decode workload: `steps` tokens as steps / k
+    m3_step_k launches of k tokens each (the state read and written once per
+    launch), captured in one CUDA graph and replayed on `stream`."""
+    launches = steps // k
+    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": launches * k, "rank": rank})
+    dec = inputs.make_decode_inputs(shape, 4 + rank_seed, device="cuda")
+    b, H = shape.batch, shape.heads
+    lay = lambda a: a[1:].reshape(launches, k, b, H, *a.shape[3:]).transpose(1, 2).contiguous()
+    X, DT, Bm, Cm, LAM, TH = (lay(dec[key]) for key in ("x", "dt", "B", "C", "lam", "theta"))
+    A, B0, X0 = dec["A"], dec["B"][0], dec["x"][0]
+    state = dec["state0"].clone()
+    del dec
+    Y = torch.empty_like(X)
+    dims = m3.scan_dims(X[0], Bm[0], 64)
+
+    # the previous-token slices are gathered once, outside the timed graph
+    prevs = [(B0, X0)] + [(Bm[i - 1][:, k - 1].contiguous(), X[i - 1][:, k - 1].contiguous())
+                          for i in range(1, launches)]
+
+    def sweep_pre():
+        for i in range(launches):
+            m3.m3_step_k(state, X[i], DT[i], A, Bm[i], Cm[i], LAM[i], TH[i], prevs[i][0], prevs[i][1], Y[i],
+                         stream=stream, dims=dims)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        sweep_pre()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep_pre()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set during the multi-token decode sweep")
+    ms = e0.elapsed_time(e1) / (reps * launches)
+    nbytes = decode_k_bytes(shape, k)
+    del X, DT, Bm, Cm, LAM, TH, Y, state, g, prevs
+    torch.cuda.empty_cache()
+    return {"workload": inputs.CONFIG_NAMES[4] + f"_R{rank}_k{k}", "tokens_per_launch": k,
+            "us_per_launch": ms * 1e3, "tokens_per_s": b * k * 1e3 / ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9,
+            "bytes_per_launch": nbytes, "graph_launches": launches, "entry": "m3_step_k"}
+
+
 def bench_decode(m3, stream, steps: int, rank_seed: int, rank: int = 1):
     """Decode sweep of the decode workload (fp32, b256 h32 P64 N64, rank R):
     `steps` consecutive m3_step calls captured in one CUDA graph and replayed
@@ -328,6 +391,7 @@ def main():
     ap.add_argument("--ref-units", type=int, default=32, help="sequences in the oracle sample (cpu_baseline)")
     ap.add_argument("--ref-budget-s", type=float, default=150.0, help="wall budget of the reference arm")
     ap.add_argument("--decode-steps", type=int, default=1024)
+    ap.add_argument("--decode-k", type=int, default=8, help="tokens per m3_step_k launch")
     ap.add_argument("--cpu-rows", type=int, default=8, help="batch rows in the oracle's cpu_baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time the cpu_baseline repeats for")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
@@ -359,6 +423,8 @@ def main():
     if args.decode_only:
         for r in (1, 4):
             print(json.dumps(bench_decode(m3, stream, args.decode_steps, rank, rank=r)), flush=True)
+            print(json.dumps(bench_decode_k(m3, stream, args.decode_steps, rank, rank=r, k=args.decode_k)),
+                  flush=True)
         return 0
 
     inp = inputs.make_scan_inputs(shape, rank_seed(args.workload, rank))
@@ -487,6 +553,11 @@ def main():
             dr = bench_decode(m3, stream, args.decode_steps, rank, rank=r)
             dr["roofline_frac"] = dr["GB_per_s"] / peaks["hbm_gbs"]
             dec[f"R{r}"] = dr
+        for r in (1, 4):
+            dk = bench_decode_k(m3, stream, args.decode_steps, rank, rank=r, k=args.decode_k)
+            dk["roofline_frac"] = dk["GB_per_s"] / peaks["hbm_gbs"]
+            dk["tokens_per_s_vs_single_step"] = dk["tokens_per_s"] / dec[f"R{r}"]["tokens_per_s"]
+            dec[f"R{r}_k{args.decode_k}"] = dk
         result["decode"] = dec
 
     if not args.no_cpu_baseline and rank == 0:

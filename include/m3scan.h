@@ -2,7 +2,8 @@
  * m3scan.h -- C ABI of libm3scan.so, the B300 (sm_103a) Mamba-3 selective
  * SSM scan: a chunked prefill (m3_scan_fwd; m3_scan_fwd_from continues a
  * sequence from a state; m3_scan_fwd_bcnorm fuses the block's B / C
- * normalisation) and a single-token decode step (m3_step).
+ * normalisation), a single-token decode step (m3_step) and a k-token decode
+ * step (m3_step_k).
  *
  * The operation (Mamba-3 summary page, "Mamba-3: Expressive SSM with MIMO"):
  * for every batch row b and head h independently, with scalar A_h < 0 and
@@ -61,7 +62,8 @@ typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
 /* Problem sizes.  batch b >= 0, seqlen T >= 0 (ignored by m3_step),
  * heads h >= 1, headdim P in [4, 256] with P % 4 == 0, dstate N in [2, 256]
  * even, rank R in [1, 8], chunk Q in {16, 32, 64, 128} (tokens per chunk of
- * the prefill; the result does not depend on it beyond rounding). */
+ * the prefill, executed as given by the chunked kernels; the result does not
+ * depend on it beyond rounding). */
 typedef struct {
     int64_t batch;
     int64_t seqlen;
@@ -86,18 +88,28 @@ typedef struct {
 #define M3_ERR_WORKSPACE (-8)   /* workspace too small */
 #define M3_ERR_VALUE (-9)       /* a scalar argument is out of range (e.g. a negative epsilon) */
 
-/* Prefill algorithms (what m3_scan_fwd would run for given dims). */
-#define M3_ALGO_NONE (-1)       /* no kernel for these dims */
-#define M3_ALGO_SEQUENTIAL 0    /* fp32 SIMT kernel, one token at a time */
-#define M3_ALGO_CHUNKED_TC 1    /* chunked tcgen05 (tensor core) kernel */
+/* Prefill algorithms (what m3_scan_fwd would run for given dims).  Both
+ * chunked kernels execute exactly d->chunk tokens per chunk. */
+#define M3_ALGO_NONE (-1)         /* no kernel for these dims */
+#define M3_ALGO_SEQUENTIAL 0      /* CUDA-core kernel, one token at a time (no chunks) */
+#define M3_ALGO_CHUNKED_TC 1      /* chunked tcgen05 (tensor core) kernel */
+#define M3_ALGO_CHUNKED_SIMT 2    /* chunked kernel on CUDA cores, fp32 arithmetic */
 
 /* Bytes of device workspace m3_scan_fwd needs for `d` (0 for every kernel of
  * this build).  Returns 0 for invalid dims as well. */
 M3_API size_t m3_scan_workspace_size(const m3_dims* d);
 
-/* Which prefill kernel m3_scan_fwd runs for `d`: M3_ALGO_CHUNKED_TC for bf16
- * inputs with P == 64, N in {64, 128}, R * Q <= 128 ... (see DESIGN), else
- * M3_ALGO_SEQUENTIAL; M3_ALGO_NONE for invalid dims. */
+/* Which prefill kernel m3_scan_fwd runs for `d` (M3_ALGO_NONE for invalid
+ * dims):
+ *   M3_ALGO_CHUNKED_TC    bf16 inputs, P == 64, N in {64, 128}, R in {1, 2, 4}
+ *                         and chunk * R == 64 (one 64-row tile per chunk:
+ *                         Q = 64, 32, 16 tokens for R = 1, 2, 4);
+ *   M3_ALGO_CHUNKED_SIMT  every other shape and chunk, fp32 or bf16, whose
+ *                         chunk fits in shared memory (inputs staged in their
+ *                         dtype: about (2 N + P) chunk R elements, the fp32
+ *                         N x P state and a 64-row block of the chunk's mask);
+ *   M3_ALGO_SEQUENTIAL    the rest (one token at a time).
+ * The result does not depend on the algorithm or the chunk beyond rounding. */
 M3_API int m3_scan_algorithm(const m3_dims* d);
 
 /* Chunked prefill from the zero state (Mamba-3 summary page §3.1-§3.3; the
@@ -179,6 +191,28 @@ M3_API int m3_step(const m3_dims* d, float* state, const void* x_t, const float*
             const float* A, const void* B_t, const void* C_t, const float* lambda_t,
             const void* theta_t, const void* prev_B, const void* prev_x, void* y_t,
             void* stream);
+
+/* k decode steps in one launch (multi-token / speculative decode): the same
+ * recurrence over k = d->seqlen consecutive tokens of every (b, h), reading
+ * and writing the state once instead of k times (Mamba-3 summary page §3.3:
+ * decode is bound by the state's bytes, so k tokens per pass over the state
+ * raise the arithmetic intensity about k-fold).  The result equals k m3_step
+ * calls, and m3_scan_fwd_from over the same k tokens.
+ *   state   [b, h, N, P]    fp32, read and overwritten with the state after
+ *                           the k-th token (complex frame), 16-byte aligned
+ *   x [b, k, h, R, P], B / C [b, k, h, R, N], theta [b, k, h, N/2] (or NULL)
+ *           dtype, token-major as in m3_scan_fwd
+ *   dt, lambda [b, k, h]    fp32 (lambda may be NULL for 1)   A [h] fp32
+ *   prev_B [b, h, R, N], prev_x [b, h, R, P]  dtype: the token before the
+ *           first one (both NULL for none)
+ *   y       [b, k, h, R, P] dtype, written
+ * d->chunk is ignored; k == 0 does nothing.  For P in {32, 64, 128}, N % 8 == 0,
+ * R in {1, 2, 4} with 16-byte aligned state, x, B, C, theta, prev_B and prev_x
+ * one kernel keeps the state in registers across the k tokens; other shapes
+ * run the continued prefill on the state in place. */
+M3_API int m3_step_k(const m3_dims* d, float* state, const void* x, const float* dt, const float* A,
+                     const void* B, const void* C, const float* lambda, const void* theta,
+                     const void* prev_B, const void* prev_x, void* y, void* stream);
 
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`: M3_OK, M3_ERR_DEVICE if a kernel reported a

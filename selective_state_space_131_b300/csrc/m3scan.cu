@@ -12,6 +12,7 @@
 #include "step_simt.cuh"
 #include "step_fast.cuh"
 #include "scan_ws.cuh"
+#include "scan_chunk.cuh"
 #include "selftest.cuh"
 
 namespace {
@@ -136,6 +137,26 @@ int dispatch_step(const m3_dims* d, float* state, const void* x_t, const float* 
     return M3_ERR_UNSUPPORTED;
 }
 
+// Geometry of the chunked CUDA-core kernel for `d` (inputs staged in their dtype).
+m3cs::Geo chunk_geo(const m3_dims* d) {
+    return m3cs::make_geo(d->seqlen, (int)d->heads, (int)d->headdim, (int)d->dstate, (int)d->rank, (int)d->chunk,
+                          d->dtype == M3_F32 ? 4 : 2);
+}
+
+template <typename T>
+int launch_chunk(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                 const float* lam, const void* theta, void* y, float* fs, const float* h0, const void* pB,
+                 const void* px, cudaStream_t s) {
+    const m3cs::Geo g = chunk_geo(d);
+    auto k = m3cs::m3_scan_chunk_kernel<T>;
+    int rc = prepare(k, (size_t)g.bytes);
+    if (rc != M3_OK) return rc;
+    k<<<(unsigned)(d->batch * d->heads), m3cs::kThreads, g.bytes, s>>>(
+        g, (const T*)x, dt, A, (const T*)B, (const T*)C, lam, (const T*)theta, (T*)y, fs, h0, (const T*)pB,
+        (const T*)px);
+    return launch_status();
+}
+
 // The decode step for the common shapes (step_fast.cuh); every tensor is
 // 16-byte aligned (checked by the caller).
 template <typename T>
@@ -166,9 +187,43 @@ int launch_step_fast(const m3_dims* d, float* state, const void* x_t, const floa
     return launch_status();
 }
 
+// The tensor-core kernel takes its shapes when the chunk is one 64-row tile
+// (Q R = 64); every other chunk runs on the chunked CUDA-core kernel when its
+// shared memory fits, else on the token-serial kernel.
+// The multi-token decode kernel for the common shapes (step_fast.cuh); every
+// tensor it reads with vector loads is 16-byte aligned (checked by the caller).
+template <typename T>
+int launch_step_k(const m3_dims* d, float* state, const void* x, const float* dt, const float* A, const void* B,
+                  const void* C, const float* lam, const void* theta, const void* prev_B, const void* prev_x, void* y,
+                  cudaStream_t s) {
+    m3fast::StepKArgs a;
+    a.H = (int)d->heads;
+    a.N = (int)d->dstate;
+    a.P = (int)d->headdim;
+    a.P4 = a.P / 4;
+    a.k = d->seqlen;
+    const int block = m3fast::threads(d->dstate, d->headdim);
+    const size_t smem = 2 * m3fast::smem_bytes(d->dstate, d->headdim, d->rank);
+    const unsigned grid = (unsigned)(d->batch * d->heads);
+#define M3_STEP_K(RR, MT)                                                                                   \
+    m3fast::m3_step_k_kernel<T, RR, MT><<<grid, block, smem, s>>>(a, state, (const T*)x, dt, A, (const T*)B,    \
+                                                                  (const T*)C, lam, (const T*)theta,            \
+                                                                  (const T*)prev_B, (const T*)prev_x, (T*)y)
+    const bool small = block <= 128;
+    switch (d->rank) {
+        case 1: if (small) M3_STEP_K(1, 128); else M3_STEP_K(1, 256); break;
+        case 2: if (small) M3_STEP_K(2, 128); else M3_STEP_K(2, 256); break;
+        case 4: if (small) M3_STEP_K(4, 128); else M3_STEP_K(4, 256); break;
+        default: return M3_ERR_UNSUPPORTED;
+    }
+#undef M3_STEP_K
+    return launch_status();
+}
+
 int scan_algorithm(const m3_dims* d) {
     if (check_dims(d, true) != M3_OK) return M3_ALGO_NONE;
-    if (m3ws::supports(*d)) return M3_ALGO_CHUNKED_TC;
+    if (m3ws::supports(*d) && d->chunk * d->rank == m3ws::kRows) return M3_ALGO_CHUNKED_TC;
+    if ((size_t)chunk_geo(d).bytes <= kMaxSmem && d->heads <= INT32_MAX) return M3_ALGO_CHUNKED_SIMT;
     SimtArgs a;
     int npt, block;
     if (!simt_geometry(d, &a, &npt, &block) || seq_smem_bytes(a) > kMaxSmem) return M3_ALGO_NONE;
@@ -223,6 +278,12 @@ int m3_scan_fwd_from(const m3_dims* d, const void* x, const float* dt, const flo
     }
     if (algo == M3_ALGO_CHUNKED_TC)
         return m3ws::launch(*d, x, dt, A, B, C, lambda, theta, initial_state, prev_B, prev_x, y, final_state, s);
+    if (algo == M3_ALGO_CHUNKED_SIMT)
+        return d->dtype == M3_F32
+                   ? launch_chunk<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state, prev_B,
+                                         prev_x, s)
+                   : launch_chunk<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state,
+                                                 prev_B, prev_x, s);
     if (d->dtype == M3_F32)
         return dispatch_seq<float>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state, prev_B, prev_x, s);
     return dispatch_seq<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, y, final_state, initial_state, prev_B, prev_x,
@@ -306,6 +367,42 @@ int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, 
         return dispatch_step<float>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x, y_t, s);
     return dispatch_step<__nv_bfloat16>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x, y_t,
                                         s);
+}
+
+int m3_step_k(const m3_dims* d, float* state, const void* x, const float* dt, const float* A, const void* B,
+              const void* C, const float* lambda, const void* theta, const void* prev_B, const void* prev_x, void* y,
+              void* stream) {
+    int rc = check_dims(d, false);
+    if (rc != M3_OK) return rc;
+    const bool work = d->batch > 0 && d->seqlen > 0;
+    if (work && (!state || !x || !dt || !A || !B || !C || !y)) return M3_ERR_NULL;
+    if ((prev_B == nullptr) != (prev_x == nullptr)) return M3_ERR_NULL;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x, B, C, theta, prev_B, prev_x, y};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt, A, lambda};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (state && !aligned16(state)) return M3_ERR_ALIGN;
+    if (!work) return M3_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m3fast::supports(d->dstate, d->headdim, d->rank)) {
+        const void* vec_ptrs[] = {state, x, B, C, theta, prev_B, prev_x};
+        bool ok16 = true;
+        for (const void* p : vec_ptrs) ok16 = ok16 && (!p || aligned16(p));
+        if (ok16)
+            return d->dtype == M3_F32
+                       ? launch_step_k<float>(d, state, x, dt, A, B, C, lambda, theta, prev_B, prev_x, y, s)
+                       : launch_step_k<__nv_bfloat16>(d, state, x, dt, A, B, C, lambda, theta, prev_B, prev_x, y, s);
+    }
+    // other shapes: the continued prefill with the state as both its initial and
+    // its final state (every prefill kernel reads a (b, h) state before it
+    // writes it, in the same CTA), in chunks of the CUDA-core kernels
+    m3_dims dc = *d;
+    dc.chunk = (16 * d->rank == m3ws::kRows) ? 32 : 16;
+    return m3_scan_fwd_from(&dc, x, dt, A, B, C, lambda, theta, state, prev_B, prev_x, y, state, nullptr, 0,
+                            stream);
 }
 
 int m3_device_status(void* stream) {

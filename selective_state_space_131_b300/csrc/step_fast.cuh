@@ -209,4 +209,138 @@ inline bool supports(int64_t N, int64_t P, int64_t R) {
 inline int threads(int64_t N, int64_t P) { return (int)((P / 4) * (N / kRPT)); }
 inline size_t smem_bytes(int64_t N, int64_t P, int64_t R) { return (size_t)(threads(N, P) / 32) * R * P * 4; }
 
+
+// ---------------------------------------------------------------------------
+// Multi-token decode (m3_step_k): k consecutive tokens of every (b, h) in one
+// launch, the state read once and written once.  The same thread tiling as
+// m3_step_fast_kernel; the state stays in registers across the k tokens, the
+// token inputs come through L1 (token j's previous token is token j - 1 of the
+// same call, or prev_B / prev_x for j = 0), and each token's y meets in a
+// double-buffered shared-memory reduction (one barrier per token).  Token
+// tensors have the prefill's token-major layout: x [b, k, h, R, P],
+// B / C [b, k, h, R, N], theta [b, k, h, N/2], dt / lambda [b, k, h].
+struct StepKArgs {
+    int H, N, P, P4;
+    int64_t k;
+};
+
+template <typename T, int R, int MAXT>
+__global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(StepKArgs a, float* __restrict__ state,
+                                                        const T* __restrict__ x, const float* __restrict__ dt,
+                                                        const float* __restrict__ A, const T* __restrict__ Bm,
+                                                        const T* __restrict__ Cm, const float* __restrict__ lam,
+                                                        const T* __restrict__ theta, const T* __restrict__ prev_B,
+                                                        const T* __restrict__ prev_x, T* __restrict__ y) {
+    extern __shared__ __align__(16) float red[];   // [2][warps][R][P]
+    const int N = a.N, P = a.P, P4 = a.P4, H = a.H;
+    if ((int)blockDim.x != P4 * (N / kRPT)) {
+        if (threadIdx.x == 0) m3::set_status(m3::kStatusBadLaunch);
+        return;
+    }
+    const int64_t unit = blockIdx.x;
+    const int64_t b = unit / H;
+    const int h = (int)(unit % H);
+    const int q = threadIdx.x % P4, g = threadIdx.x / P4;
+    const int n0 = g * kRPT, p0 = 4 * q;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    float* st = state + unit * (int64_t)N * P + (int64_t)n0 * P + p0;
+
+    float4 hs[kRPT];
+#pragma unroll
+    for (int i = 0; i < kRPT; ++i) hs[i] = __ldcs(reinterpret_cast<const float4*>(st + (int64_t)i * P));
+    const float A_h = __ldg(A + h);
+
+    for (int64_t j = 0; j < a.k; ++j) {
+        const int64_t tj = (b * a.k + j) * H + h;          // token j of this (b, h) in [b, k, h]
+        const float d = __ldg(dt + tj);
+        const float l = lam ? __ldg(lam + tj) : 1.0f;
+        const float alpha = expf(d * A_h);
+        const float beta = (1.0f - l) * d * alpha;
+        const float gamma = l * d;
+        // the previous token's B and x: token j - 1 of this call, or the caller's
+        const bool has_prev = (j > 0) || (prev_B != nullptr);
+        const T* pxp = j > 0 ? x + (tj - H) * R * P : (has_prev ? prev_x + unit * R * P : nullptr);
+        const T* pBp = j > 0 ? Bm + (tj - H) * R * N + n0 : (has_prev ? prev_B + unit * R * N + n0 : nullptr);
+        float xr[R][4], pxr[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            Vec<T>::ld4(x + (tj * R + r) * P + p0, xr[r]);
+            if (has_prev) {
+                Vec<T>::ld4(pxp + r * P + p0, pxr[r]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) pxr[r][jj] = 0.0f;
+            }
+        }
+        const T* Bp = Bm + tj * R * N + n0;
+        const T* Cp = Cm + tj * R * N + n0;
+        float cs[kRPT / 2], sn[kRPT / 2];
+        {
+            float th[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (theta) Vec<T>::ld4(theta + tj * (N / 2) + n0 / 2, th);
+#pragma unroll
+            for (int m = 0; m < kRPT / 2; ++m) __sincosf(reduce_2pi(th[m]), &sn[m], &cs[m]);
+        }
+        float yp[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) yp[r][jj] = 0.0f;
+#pragma unroll
+        for (int m = 0; m < kRPT / 2; ++m) {
+            float* h0 = reinterpret_cast<float*>(&hs[2 * m]);
+            float* h1 = reinterpret_cast<float*>(&hs[2 * m + 1]);
+            float2 br[R], pbr[R], cr[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                br[r] = Vec<T>::ld2(Bp + r * N + 2 * m);
+                cr[r] = Vec<T>::ld2(Cp + r * N + 2 * m);
+                pbr[r] = has_prev ? Vec<T>::ld2(pBp + r * N + 2 * m) : make_float2(0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                float v0 = 0.0f, v1 = 0.0f, u0 = 0.0f, u1 = 0.0f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    v0 = fmaf(pbr[r].x, pxr[r][jj], v0);
+                    v1 = fmaf(pbr[r].y, pxr[r][jj], v1);
+                    u0 = fmaf(br[r].x, xr[r][jj], u0);
+                    u1 = fmaf(br[r].y, xr[r][jj], u1);
+                }
+                const float z0 = fmaf(alpha, h0[jj], beta * v0);
+                const float z1 = fmaf(alpha, h1[jj], beta * v1);
+                const float o0 = fmaf(gamma, u0, fmaf(cs[m], z0, -sn[m] * z1));
+                const float o1 = fmaf(gamma, u1, fmaf(sn[m], z0, cs[m] * z1));
+                h0[jj] = o0;
+                h1[jj] = o1;
+#pragma unroll
+                for (int r = 0; r < R; ++r) yp[r][jj] = fmaf(cr[r].x, o0, fmaf(cr[r].y, o1, yp[r][jj]));
+            }
+        }
+        // y of token j: lanes P4 apart, then the warps through shared memory
+#pragma unroll
+        for (int o = P4; o < 32; o <<= 1)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) yp[r][jj] += __shfl_xor_sync(0xffffffffu, yp[r][jj], o);
+        float* rb = red + (j & 1) * nwarps * R * P;
+        if (lane < P4) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                *reinterpret_cast<float4*>(rb + (warp * R + r) * P + p0) =
+                    make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < R * P; e += blockDim.x) {
+            float acc = 0.0f;
+            for (int w = 0; w < nwarps; ++w) acc += rb[w * R * P + e];
+            Vec<T>::st(y + tj * R * P + e, acc);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kRPT; ++i) __stcs(reinterpret_cast<float4*>(st + (int64_t)i * P), hs[i]);
+}
+
 }  // namespace m3fast

@@ -25,7 +25,7 @@ M3_OK = 0
 M3_ERR_NULL, M3_ERR_SHAPE, M3_ERR_DTYPE, M3_ERR_ALIGN = -1, -2, -3, -4
 M3_ERR_CUDA, M3_ERR_UNSUPPORTED, M3_ERR_DEVICE, M3_ERR_WORKSPACE = -5, -6, -7, -8
 M3_ERR_VALUE = -9
-M3_ALGO_NONE, M3_ALGO_SEQUENTIAL, M3_ALGO_CHUNKED_TC = -1, 0, 1
+M3_ALGO_NONE, M3_ALGO_SEQUENTIAL, M3_ALGO_CHUNKED_TC, M3_ALGO_CHUNKED_SIMT = -1, 0, 1, 2
 
 
 class m3_dims(ctypes.Structure):
@@ -48,6 +48,8 @@ _lib.m3_scan_fwd_bcnorm.argtypes = [_dp] + [_vp] * 11 + [ctypes.c_float] + [_vp]
 _lib.m3_scan_fwd_bcnorm.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
+_lib.m3_step_k.argtypes = [_dp] + [_vp] * 11 + [_vp]
+_lib.m3_step_k.restype = ctypes.c_int
 _lib.m3_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _vp]
 _lib.m3_selftest_wait_timeout.restype = ctypes.c_int
 _lib.m3_device_status.argtypes = [_vp]
@@ -181,6 +183,25 @@ def m3_step(state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, 
                       _ptr(lam_t), _ptr(theta_t), _ptr(prev_B), _ptr(prev_x), _ptr(y_t), _stream(stream))
     if rc != M3_OK:
         raise M3Error(rc, "m3_step")
+
+
+def m3_step_k(state, x, dt, A, B, C, lam, theta, prev_B, prev_x, y, stream=None,
+              dims: m3_dims | None = None) -> None:
+    """k decode steps in one launch: x [b,k,h,R,P], dt / lam [b,k,h],
+    B / C [b,k,h,R,N], theta [b,k,h,N/2] (token-major, as for the prefill);
+    updates state [b,h,N,P] in place and writes y [b,k,h,R,P].  Raises M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, 64)
+    rc = _lib.m3_step_k(ctypes.byref(dims), _ptr(state), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam),
+                        _ptr(theta), _ptr(prev_B), _ptr(prev_x), _ptr(y), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_step_k")
+
+
+def raw_step_k(dims: m3_dims, ptrs, stream=None) -> int:
+    """Direct call with raw addresses (state, x, dt, A, B, C, lam, theta, prev_B,
+    prev_x, y); returns the status code."""
+    return int(_lib.m3_step_k(ctypes.byref(dims), *ptrs, stream))
 
 
 def m3_selftest_wait_timeout(budget_cycles: int, stream=None) -> int:

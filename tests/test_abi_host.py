@@ -32,7 +32,7 @@ def declared_symbols():
 
 def test_every_declared_symbol_is_exported(m3):
     names = declared_symbols()
-    assert {"m3_scan_fwd", "m3_step", "m3_scan_workspace_size", "m3_status_string"} <= set(names)
+    assert {"m3_scan_fwd", "m3_step", "m3_step_k", "m3_scan_workspace_size", "m3_status_string"} <= set(names)
     lib = ctypes.CDLL(m3.LIBRARY_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -97,7 +97,20 @@ def test_step_validation(m3):
 
 def test_algorithm_selection(m3):
     assert m3.m3_scan_algorithm(_dims(m3, dstate=63)) == m3.M3_ALGO_NONE
-    assert m3.m3_scan_algorithm(_dims(m3, dtype=m3.M3_F32)) == m3.M3_ALGO_SEQUENTIAL
+    # the tensor-core kernel takes bf16, P = 64, N in {64, 128}, R in {1, 2, 4} when
+    # the chunk is its 64-row tile (chunk * R == 64)
+    for n in (64, 128):
+        for r in (1, 2, 4):
+            assert m3.m3_scan_algorithm(_dims(m3, dstate=n, rank=r, chunk=64 // r)) == m3.M3_ALGO_CHUNKED_TC
+    # any other chunk is executed as given by the chunked CUDA-core kernel
+    assert m3.m3_scan_algorithm(_dims(m3, chunk=32)) == m3.M3_ALGO_CHUNKED_SIMT
+    assert m3.m3_scan_algorithm(_dims(m3, chunk=128)) == m3.M3_ALGO_CHUNKED_SIMT
+    assert m3.m3_scan_algorithm(_dims(m3, rank=4, chunk=64)) == m3.M3_ALGO_CHUNKED_SIMT
+    assert m3.m3_scan_algorithm(_dims(m3, dtype=m3.M3_F32)) == m3.M3_ALGO_CHUNKED_SIMT
+    assert m3.m3_scan_algorithm(_dims(m3, headdim=16, dstate=16, chunk=32, dtype=m3.M3_F32)) == \
+        m3.M3_ALGO_CHUNKED_SIMT
+    # a chunk too large for shared memory falls back to the token-serial kernel
+    assert m3.m3_scan_algorithm(_dims(m3, rank=8, chunk=128, dtype=m3.M3_F32)) == m3.M3_ALGO_SEQUENTIAL
     assert m3.m3_scan_workspace_size(_dims(m3)) == 0
 
 
@@ -139,8 +152,9 @@ def test_scan_bcnorm_validation(m3):
         assert m3.raw_scan_fwd_bcnorm(d, _bcnorm_ptrs(**{k: FAKE + 2}), 1e-6) == m3.M3_ERR_ALIGN
     for eps in (-1e-6, float("inf"), float("nan")):
         assert m3.raw_scan_fwd_bcnorm(d, _bcnorm_ptrs(), eps) == m3.M3_ERR_VALUE
-    # only the tensor-core kernel's shapes take the fused normalisation
+    # only the tensor-core kernel's shapes and chunk take the fused normalisation
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, dtype=m3.M3_F32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
+    assert m3.raw_scan_fwd_bcnorm(_dims(m3, chunk=32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, headdim=32), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_UNSUPPORTED
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, dstate=7), _bcnorm_ptrs(), 1e-6) == m3.M3_ERR_SHAPE
     assert m3.raw_scan_fwd_bcnorm(_dims(m3, batch=0), _bcnorm_ptrs(x=None, y=None), 1e-6) == m3.M3_OK
@@ -160,3 +174,18 @@ def test_binding_rejects_strided_tensors(m3):
         m3._ptr(t.t())                  # a transposed view is not C-contiguous
     with pytest.raises(ValueError):
         m3._ptr(torch.zeros(3, 5, 2)[:, 1])
+
+
+def test_step_k_validation(m3):
+    # pointers in the order (state, x, dt, A, B, C, lam, theta, pB, px, y)
+    d = _dims(m3, seqlen=8)
+    assert m3.raw_step_k(d, _step_ptrs(state=None)) == m3.M3_ERR_NULL
+    assert m3.raw_step_k(d, _step_ptrs(x=None)) == m3.M3_ERR_NULL
+    assert m3.raw_step_k(d, _step_ptrs(pB=None)) == m3.M3_ERR_NULL    # prev_B and prev_x go together
+    assert m3.raw_step_k(_dims(m3, seqlen=8, dstate=5), _step_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_step_k(_dims(m3, seqlen=-1), _step_ptrs()) == m3.M3_ERR_SHAPE
+    assert m3.raw_step_k(d, _step_ptrs(px=FAKE + 1)) == m3.M3_ERR_ALIGN
+    assert m3.raw_step_k(d, _step_ptrs(state=FAKE + 4)) == m3.M3_ERR_ALIGN
+    # no token or no batch row: nothing to do, nothing launched
+    assert m3.raw_step_k(_dims(m3, seqlen=0), _step_ptrs()) == m3.M3_OK
+    assert m3.raw_step_k(_dims(m3, seqlen=8, batch=0), _step_ptrs()) == m3.M3_OK

@@ -67,7 +67,7 @@ SMALL = [
 
 @pytest.mark.parametrize("T,N,R,lam,th", SMALL, ids=lambda v: str(v))
 def test_bcnorm_small(m3, T, N, R, lam, th):
-    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=N, rank=R, chunk=64, dtype="bf16",
+    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=N, rank=R, chunk=64 // R, dtype="bf16",
                              with_lambda=lam, with_theta=th)
     ey, ef = run_and_check(m3, shape, 3000 + T + N + R)
     print(f"T{T} N{N} R{R} lam{lam} th{th}: y {ey:.2e} state {ef:.2e}")

@@ -1,5 +1,5 @@
-"""GPU parity of the SIMT kernels (sequential prefill, decode step) against
-the fp64 oracle, through the C ABI."""
+"""GPU parity of the CUDA-core kernels (the chunked prefill, the token-serial
+prefill, the generic decode step) against the fp64 oracle, through the C ABI."""
 import numpy as np
 import pytest
 import torch
@@ -35,8 +35,9 @@ def check_scan(m3, shape, seed, expect_algo=None):
 
 
 def test_config0_tiny_f32(m3):
-    """The tiny SISO fp32 workload (b1 h2 T256 P16 N16 Q32, seed 0) at 1e-4."""
-    ey, ef = check_scan(m3, inputs.CONFIGS[0], 0, m3.M3_ALGO_SEQUENTIAL)
+    """The tiny SISO fp32 workload (b1 h2 T256 P16 N16, seed 0) at 1e-4, in
+    chunks of 32 tokens on the chunked CUDA-core kernel."""
+    ey, ef = check_scan(m3, inputs.CONFIGS[0], 0, m3.M3_ALGO_CHUNKED_SIMT)
     print(f"config0: y {ey:.2e} state {ef:.2e}")
 
 
@@ -51,15 +52,12 @@ SMALL = [
 
 
 @pytest.mark.parametrize("kw", SMALL, ids=lambda k: "b{batch}T{seqlen}h{heads}P{headdim}N{dstate}R{rank}".format(**k))
+@pytest.mark.parametrize("chunk", [16, 32, 128])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_sequential_scan_shapes(m3, kw, dtype):
-    shape = inputs.ScanShape(chunk=32, dtype=dtype, **kw)
-    dims = m3.scan_dims(*(torch.empty(shape.batch, shape.seqlen, shape.heads, shape.rank, s,
-                                      dtype=torch.float32 if dtype == "f32" else torch.bfloat16)
-                          for s in (shape.headdim, shape.dstate)), 32)
-    if dtype == "bf16" and m3.m3_scan_algorithm(dims) != m3.M3_ALGO_SEQUENTIAL:
-        pytest.skip("covered by the tensor-core tests")
-    check_scan(m3, shape, 100 + kw["seqlen"])
+def test_cuda_core_scan_shapes(m3, kw, chunk, dtype):
+    shape = inputs.ScanShape(chunk=chunk, dtype=dtype, **kw)
+    ey, ef = check_scan(m3, shape, 100 + kw["seqlen"])
+    print(f"{kw} Q{chunk} {dtype}: y {ey:.2e} state {ef:.2e}")
 
 
 def test_no_lambda_no_theta(m3):
@@ -148,7 +146,7 @@ def test_decode_continues_prefill(m3):
     assert max_rel(state.cpu(), fr) <= 1e-4
 
 
-def test_sequential_scan_is_deterministic(m3):
+def test_chunked_scan_is_deterministic(m3):
     shape = inputs.ScanShape(batch=2, seqlen=64, heads=2, headdim=32, dstate=16, rank=2, chunk=32, dtype="f32")
     d = dev(inputs.make_scan_inputs(shape, 4))
     y1, f1 = gpu_scan(m3, d, 32)

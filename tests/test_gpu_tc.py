@@ -40,38 +40,35 @@ def run_and_check(m3, shape, seed, bsel=None, hsel=None, tol=None):
 
 
 SMALL = [
-    # (T, N, R, chunk, lambda, theta): several chunks, ragged tails, one token,
-    # exactly one chunk, every (N, R) the tensor-core kernel takes, with and
-    # without lambda / theta
-    (209, 64, 1, 64, True, True),
-    (209, 64, 1, 128, True, True),
-    (64, 64, 1, 64, True, True),
-    (65, 64, 1, 64, True, True),
-    (1, 64, 1, 64, True, True),
-    (37, 64, 1, 64, True, True),
-    (209, 128, 1, 64, True, True),
-    (209, 128, 1, 64, False, False),
-    (209, 64, 1, 64, False, False),
-    (209, 64, 1, 64, True, False),
-    (209, 64, 1, 64, False, True),
-    (130, 64, 2, 64, True, True),
-    (130, 64, 4, 64, True, True),
-    (130, 64, 4, 16, True, True),
-    (17, 64, 4, 16, True, True),
-    (130, 128, 2, 32, True, True),
-    (130, 128, 4, 64, True, False),
-    (130, 128, 4, 64, True, True),
-    (513, 64, 1, 64, True, True),
+    # (T, N, R, lambda, theta): several chunks, ragged tails, one token, exactly
+    # one chunk, every (N, R) the tensor-core kernel takes, with and without
+    # lambda / theta.  The chunk is the kernel's 64-row tile: 64 / R tokens.
+    (209, 64, 1, True, True),
+    (64, 64, 1, True, True),
+    (65, 64, 1, True, True),
+    (1, 64, 1, True, True),
+    (37, 64, 1, True, True),
+    (209, 128, 1, True, True),
+    (209, 128, 1, False, False),
+    (209, 64, 1, False, False),
+    (209, 64, 1, True, False),
+    (209, 64, 1, False, True),
+    (130, 64, 2, True, True),
+    (130, 64, 4, True, True),
+    (17, 64, 4, True, True),
+    (130, 128, 2, True, True),
+    (130, 128, 4, True, False),
+    (130, 128, 4, True, True),
+    (513, 64, 1, True, True),
 ]
 
 
-@pytest.mark.parametrize("T,N,R,chunk,lam,th", SMALL,
-                         ids=lambda v: str(v))
-def test_tc_small(m3, T, N, R, chunk, lam, th):
-    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=N, rank=R, chunk=chunk, dtype="bf16",
+@pytest.mark.parametrize("T,N,R,lam,th", SMALL, ids=lambda v: str(v))
+def test_tc_small(m3, T, N, R, lam, th):
+    shape = inputs.ScanShape(batch=2, seqlen=T, heads=3, headdim=64, dstate=N, rank=R, chunk=64 // R, dtype="bf16",
                              with_lambda=lam, with_theta=th)
     ey, ef = run_and_check(m3, shape, 1000 + T + N + R)
-    print(f"T{T} N{N} R{R} Q{chunk} lam{lam} th{th}: y {ey:.2e} state {ef:.2e}")
+    print(f"T{T} N{N} R{R} lam{lam} th{th}: y {ey:.2e} state {ef:.2e}")
 
 
 # Full-size units checked: every (batch, head) sequence of the SSD-equivalent and
@@ -86,23 +83,35 @@ FULL_SEL = {1: (list(range(8)), list(range(32))),
 @pytest.mark.parametrize("cfg", [1, 2, 3])
 def test_tc_full_size_workloads(m3, cfg):
     """The bf16 workloads at full size, in the launch configuration the bench
-    times (the tensor-core kernel), checked against the oracle on the units of
-    FULL_SEL."""
+    times (the tensor-core kernel; for the MIMO workload its 16-token chunk, the
+    64-row tile at R = 4), checked against the oracle on the units of FULL_SEL."""
     shape = inputs.CONFIGS[cfg]
+    shape = inputs.ScanShape(**{**shape.__dict__, "chunk": 64 // shape.rank})
     bsel, hsel = FULL_SEL[cfg]
     ey, ef = run_and_check(m3, shape, cfg, bsel, hsel)
     print(f"config {cfg}: y {ey:.2e} state {ef:.2e}")
 
 
-def test_chunk_invariance(m3):
-    """The result does not depend on the chunk size beyond rounding."""
+def test_chunk_invariance_across_kernels(m3):
+    """The result does not depend on the chunk beyond rounding: the same bf16
+    inputs through the tensor-core kernel (chunk 64) and the chunked CUDA-core
+    kernel at chunks 16, 32 and 128 -- four executions that really tile the
+    sequence differently -- each match the oracle, and each other."""
     shape = inputs.ScanShape(batch=2, seqlen=300, heads=2, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16")
-    d = dev(inputs.make_scan_inputs(shape, 5))
-    y64, f64 = gpu_scan(m3, d, 64)
-    y128, f128 = gpu_scan(m3, d, 128)
-    torch.cuda.synchronize()
-    assert max_rel(y64.float().cpu(), y128.float().cpu()) <= 2e-2
-    assert max_rel(f64.cpu(), f128.cpu()) <= 2e-2
+    inp = inputs.make_scan_inputs(shape, 5)
+    d = dev(inp)
+    yr, fr = oracle_scan(inp)
+    outs = {}
+    for q, algo in [(64, m3.M3_ALGO_CHUNKED_TC), (16, m3.M3_ALGO_CHUNKED_SIMT), (32, m3.M3_ALGO_CHUNKED_SIMT),
+                    (128, m3.M3_ALGO_CHUNKED_SIMT)]:
+        assert m3.m3_scan_algorithm(m3.scan_dims(d["x"], d["B"], q)) == algo
+        y, f = gpu_scan(m3, d, q)
+        torch.cuda.synchronize()
+        outs[q] = (y.float().cpu(), f.cpu())
+        assert max_rel(outs[q][0], yr) <= 2e-2 and max_rel(outs[q][1], fr) <= 2e-2, q
+    for q in (16, 32, 128):
+        assert max_rel(outs[q][0], outs[64][0]) <= 2e-2
+        assert max_rel(outs[q][1], outs[64][1]) <= 2e-2
 
 
 def test_tc_prefill_then_decode(m3):
