@@ -2,8 +2,8 @@
  * m3scan.h -- C ABI of libm3scan.so, the B300 (sm_103a) Mamba-3 selective
  * SSM scan: a chunked prefill (m3_scan_fwd; m3_scan_fwd_from continues a
  * sequence from a state; m3_scan_fwd_bcnorm fuses the block's B / C
- * normalisation), a single-token decode step (m3_step) and a k-token decode
- * step (m3_step_k).
+ * normalisation), its backward pass (m3_scan_bwd), a single-token decode
+ * step (m3_step) and a k-token decode step (m3_step_k).
  *
  * The operation (Mamba-3 summary page, "Mamba-3: Expressive SSM with MIMO"):
  * for every batch row b and head h independently, with scalar A_h < 0 and
@@ -29,7 +29,8 @@
  *    element size; the fp32 state / final_state must be 16-byte aligned, and
  *    the tensor-core prefill (M3_ALGO_CHUNKED_TC) also needs x, B, C, theta
  *    and y 16-byte aligned (it returns M3_ERR_ALIGN otherwise).
- *    The library never allocates device memory and never frees a pointer.
+ *    The library never allocates device memory and never frees a pointer;
+ *    scratch (m3_scan_bwd) is a caller-owned workspace.
  *  - Arguments are validated on the host before any launch; on error nothing
  *    is launched and a negative status is returned.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -95,8 +96,8 @@ typedef struct {
 #define M3_ALGO_CHUNKED_TC 1      /* chunked tcgen05 (tensor core) kernel */
 #define M3_ALGO_CHUNKED_SIMT 2    /* chunked kernel on CUDA cores, fp32 arithmetic */
 
-/* Bytes of device workspace m3_scan_fwd needs for `d` (0 for every kernel of
- * this build).  Returns 0 for invalid dims as well. */
+/* Bytes of device workspace m3_scan_fwd needs for `d` (0 for every forward
+ * kernel of this build).  Returns 0 for invalid dims as well. */
 M3_API size_t m3_scan_workspace_size(const m3_dims* d);
 
 /* Which prefill kernel m3_scan_fwd runs for `d` (M3_ALGO_NONE for invalid
@@ -191,6 +192,40 @@ M3_API int m3_step(const m3_dims* d, float* state, const void* x_t, const float*
             const float* A, const void* B_t, const void* C_t, const float* lambda_t,
             const void* theta_t, const void* prev_B, const void* prev_x, void* y_t,
             void* stream);
+
+/* Bytes of device workspace m3_scan_bwd needs for `d` (0 when m3_scan_bwd does
+ * not take these dims): the chunk states of every (b, h), (ceil(T / chunk) + 1)
+ * N P fp32 each, the angles at every chunk start and one float per (b, h). */
+M3_API size_t m3_scan_bwd_workspace_size(const m3_dims* d);
+
+/* Backward pass of the prefill from the zero state (m3_scan_fwd): given the
+ * upstream gradients dy of y and dfinal of final_state, the gradients of
+ *   L = <dy, y> + <dfinal, final_state>
+ * with respect to every input, for training (the recompute-in-backward of the
+ * Mamba-1 review page, "hardware-aware algorithm" step 4; the chunked training
+ * path of "Foundation Model Engineering" ch. 20.2).  A first pass recomputes
+ * the chunk states into the workspace; a second pass walks the chunks in
+ * reverse and differentiates the chunked form (the intra-chunk mask, the
+ * inter-chunk term, the state update, the trapezoid weights, the cumulative
+ * rotation); a third sums dA over the batch.  fp32 arithmetic on CUDA cores,
+ * deterministic (fixed-order sums).
+ *   x, dt, A, B, C, lambda, theta   the forward's inputs (as in m3_scan_fwd)
+ *   dy      [b, T, h, R, P]  dtype        dfinal [b, h, N, P] fp32 or NULL (0)
+ *   dx      [b, T, h, R, P]  dtype        ddt    [b, T, h]    fp32
+ *   dA      [h]              fp32 (summed over the batch and time)
+ *   dB, dC  [b, T, h, R, N]  dtype
+ *   dlambda [b, T, h] fp32 (required when lambda is given, else ignored)
+ *   dtheta  [b, T, h, N/2] dtype (required when theta is given, else ignored)
+ *   workspace: >= m3_scan_bwd_workspace_size(d) bytes, 256-byte aligned
+ *           (M3_ERR_WORKSPACE if smaller).
+ * Takes chunk * R <= 64 rows per chunk (M3_ERR_UNSUPPORTED otherwise, or when
+ * a chunk does not fit in shared memory: N = P = 64 takes chunk 64 at R = 1).
+ * The chunk changes only the rounding.  T == 0 writes dA = 0 only. */
+M3_API int m3_scan_bwd(const m3_dims* d, const void* x, const float* dt, const float* A,
+                       const void* B, const void* C, const float* lambda, const void* theta,
+                       const void* dy, const float* dfinal, void* dx, float* ddt, float* dA,
+                       void* dB, void* dC, float* dlambda, void* dtheta, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* k decode steps in one launch (multi-token / speculative decode): the same
  * recurrence over k = d->seqlen consecutive tokens of every (b, h), reading

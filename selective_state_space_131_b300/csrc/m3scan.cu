@@ -13,6 +13,7 @@
 #include "step_fast.cuh"
 #include "scan_ws.cuh"
 #include "scan_chunk.cuh"
+#include "scan_bwd.cuh"
 #include "selftest.cuh"
 
 namespace {
@@ -196,14 +197,18 @@ template <typename T>
 int launch_step_k(const m3_dims* d, float* state, const void* x, const float* dt, const float* A, const void* B,
                   const void* C, const float* lam, const void* theta, const void* prev_B, const void* prev_x, void* y,
                   cudaStream_t s) {
-    m3fast::StepKArgs a;
-    a.H = (int)d->heads;
-    a.N = (int)d->dstate;
-    a.P = (int)d->headdim;
-    a.P4 = a.P / 4;
-    a.k = d->seqlen;
+    const m3fast::StepKArgs a = m3fast::stepk_layout((int)d->heads, (int)d->dstate, (int)d->headdim, (int)d->rank,
+                                                     d->seqlen, (int)sizeof(T));
     const int block = m3fast::threads(d->dstate, d->headdim);
-    const size_t smem = 2 * m3fast::smem_bytes(d->dstate, d->headdim, d->rank);
+    const size_t smem = m3fast::stepk_smem(a, (int)d->rank);
+    int rc = M3_OK;
+    switch (d->rank) {
+        case 1: rc = prepare(m3fast::m3_step_k_kernel<T, 1, 128>, smem); if (rc == M3_OK) rc = prepare(m3fast::m3_step_k_kernel<T, 1, 256>, smem); break;
+        case 2: rc = prepare(m3fast::m3_step_k_kernel<T, 2, 128>, smem); if (rc == M3_OK) rc = prepare(m3fast::m3_step_k_kernel<T, 2, 256>, smem); break;
+        case 4: rc = prepare(m3fast::m3_step_k_kernel<T, 4, 128>, smem); if (rc == M3_OK) rc = prepare(m3fast::m3_step_k_kernel<T, 4, 256>, smem); break;
+        default: return M3_ERR_UNSUPPORTED;
+    }
+    if (rc != M3_OK) return rc;
     const unsigned grid = (unsigned)(d->batch * d->heads);
 #define M3_STEP_K(RR, MT)                                                                                   \
     m3fast::m3_step_k_kernel<T, RR, MT><<<grid, block, smem, s>>>(a, state, (const T*)x, dt, A, (const T*)B,    \
@@ -230,9 +235,78 @@ int scan_algorithm(const m3_dims* d) {
     return M3_ALGO_SEQUENTIAL;
 }
 
+// The backward pass: chunk * R <= 64 rows, and both passes' shared memory fits.
+m3bwd::Geo bwd_geo(const m3_dims* d) {
+    return m3bwd::make_geo(d->seqlen, (int)d->heads, (int)d->headdim, (int)d->dstate, (int)d->rank, (int)d->chunk);
+}
+bool bwd_supported(const m3_dims* d) {
+    if (d->chunk * d->rank > 64) return false;
+    const m3bwd::Geo g = bwd_geo(d);
+    return (size_t)g.bytes <= kMaxSmem && (size_t)g.c_bytes <= kMaxSmem;
+}
+
+template <typename T>
+int launch_bwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+               const float* lam, const void* theta, const void* dy, const float* dfinal, void* dx, float* ddt,
+               float* dA, void* dB, void* dC, float* dlam, void* dtheta, void* ws, cudaStream_t s) {
+    const m3bwd::Geo g = bwd_geo(d);
+    const int64_t units = d->batch * d->heads;
+    const m3bwd::Work w = m3bwd::work_split(ws, units, g);
+    auto k1 = m3bwd::m3_bwd_ckpt_kernel<T>;
+    auto k2 = m3bwd::m3_bwd_chunk_kernel<T>;
+    int rc = prepare(k1, (size_t)g.c_bytes);
+    if (rc == M3_OK) rc = prepare(k2, (size_t)g.bytes);
+    if (rc != M3_OK) return rc;
+    k1<<<(unsigned)units, m3bwd::kThreads, g.c_bytes, s>>>(g, w, (const T*)x, dt, A, (const T*)B, lam,
+                                                           (const T*)theta);
+    k2<<<(unsigned)units, m3bwd::kThreads, g.bytes, s>>>(g, w, (const T*)x, dt, A, (const T*)B, (const T*)C, lam,
+                                                         (const T*)theta, (const T*)dy, dfinal, (T*)dx, ddt, (T*)dB,
+                                                         (T*)dC, dlam, (T*)dtheta);
+    m3bwd::m3_bwd_dA_kernel<<<(unsigned)((d->heads + 127) / 128), 128, 0, s>>>(w.dA, d->batch, (int)d->heads, dA);
+    return launch_status();
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t m3_scan_bwd_workspace_size(const m3_dims* d) {
+    if (check_dims(d, true) != M3_OK || !bwd_supported(d)) return 0;
+    return m3bwd::work_bytes(d->batch * d->heads, bwd_geo(d));
+}
+
+int m3_scan_bwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                const float* lambda, const void* theta, const void* dy, const float* dfinal, void* dx, float* ddt,
+                float* dA, void* dB, void* dC, float* dlambda, void* dtheta, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    int rc = check_dims(d, true);
+    if (rc != M3_OK) return rc;
+    const bool has_tokens = d->batch > 0 && d->seqlen > 0;
+    if (!dA) return M3_ERR_NULL;
+    if (has_tokens && (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dB || !dC)) return M3_ERR_NULL;
+    if (has_tokens && ((lambda != nullptr && !dlambda) || (theta != nullptr && !dtheta))) return M3_ERR_NULL;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x, B, C, theta, dy, dx, dB, dC, dtheta};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt, A, lambda, dfinal, ddt, dA, dlambda};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (!bwd_supported(d)) return M3_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!has_tokens) {
+        // no token: y does not exist and the final state is zero whatever the
+        // inputs, so every gradient is zero; only dA has elements
+        return cudaMemsetAsync(dA, 0, sizeof(float) * d->heads, s) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+    }
+    const size_t need = m3bwd::work_bytes(d->batch * d->heads, bwd_geo(d));
+    if (!workspace || workspace_bytes < need) return M3_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+    return d->dtype == M3_F32 ? launch_bwd<float>(d, x, dt, A, B, C, lambda, theta, dy, dfinal, dx, ddt, dA, dB, dC,
+                                                  dlambda, dtheta, workspace, s)
+                              : launch_bwd<__nv_bfloat16>(d, x, dt, A, B, C, lambda, theta, dy, dfinal, dx, ddt, dA,
+                                                          dB, dC, dlambda, dtheta, workspace, s);
+}
 
 size_t m3_scan_workspace_size(const m3_dims* d) {
     (void)d;

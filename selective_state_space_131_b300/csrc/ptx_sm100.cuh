@@ -123,6 +123,10 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid
                  "r"(valid ? 4 : 0)
                  : "memory");
 }
+// 16-byte async copy global -> shared, bypassing L1 (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 

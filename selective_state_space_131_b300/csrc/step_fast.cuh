@@ -17,6 +17,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx_sm100.cuh"
 
 namespace m3fast {
 
@@ -212,16 +213,65 @@ inline size_t smem_bytes(int64_t N, int64_t P, int64_t R) { return (size_t)(thre
 
 // ---------------------------------------------------------------------------
 // Multi-token decode (m3_step_k): k consecutive tokens of every (b, h) in one
-// launch, the state read once and written once.  The same thread tiling as
-// m3_step_fast_kernel; the state stays in registers across the k tokens, the
-// token inputs come through L1 (token j's previous token is token j - 1 of the
-// same call, or prev_B / prev_x for j = 0), and each token's y meets in a
-// double-buffered shared-memory reduction (one barrier per token).  Token
-// tensors have the prefill's token-major layout: x [b, k, h, R, P],
+// launch, the state read once and written once.  The thread tiling of
+// m3_step_fast_kernel; the state stays in registers across the k tokens.  The
+// tokens' inputs are staged in shared memory in groups of kGroup with 16-byte
+// cp.async copies, so the global latency is paid once per group rather than
+// per token: group 0 (and the caller's previous token) before the state loads,
+// group g + 1 as soon as the first token of group g is done (two buffers; the
+// previous token of group g's first token is the last of group g - 1).  Each
+// token's y meets in a double-buffered shared-memory reduction (one barrier per
+// token).  Token tensors have the prefill's token-major layout: x [b, k, h, R, P],
 // B / C [b, k, h, R, N], theta [b, k, h, N/2], dt / lambda [b, k, h].
+constexpr int kGroup = 8;
+
 struct StepKArgs {
     int H, N, P, P4;
     int64_t k;
+    // staging layout (bytes): per token x | B | C | theta | dt, lambda; the
+    // previous-token slot x | B; nbuf group buffers of kGroup tokens
+    int xb, nb, kb, tokb, nbuf;
+};
+
+inline StepKArgs stepk_layout(int H, int N, int P, int R, int64_t k, int es) {
+    auto up16 = [](int v) { return (v + 15) & ~15; };
+    StepKArgs a;
+    a.H = H; a.N = N; a.P = P; a.P4 = P / 4; a.k = k;
+    a.xb = R * P * es;
+    a.nb = up16(R * N * es);
+    a.kb = up16((N / 2) * es);
+    a.tokb = a.xb + 2 * a.nb + a.kb + 16;
+    a.nbuf = k > kGroup ? 2 : 1;
+    return a;
+}
+// Dynamic shared memory of m3_step_k_kernel: the y reduction (2 x warps x R x P
+// floats), the previous-token slot and the group buffers.
+inline size_t stepk_smem(const StepKArgs& a, int R) {
+    const int warps = (a.P4 * (a.N / kRPT)) / 32;
+    return (size_t)2 * warps * R * a.P * 4 + (size_t)(a.xb + a.nb) + (size_t)a.nbuf * kGroup * a.tokb;
+}
+
+template <typename T>
+struct SVec;
+template <>
+struct SVec<float> {
+    static __device__ __forceinline__ void ld4(const uint8_t* p, float (&o)[4]) {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    }
+    static __device__ __forceinline__ float2 ld2(const uint8_t* p) { return *reinterpret_cast<const float2*>(p); }
+};
+template <>
+struct SVec<__nv_bfloat16> {
+    static __device__ __forceinline__ void ld4(const uint8_t* p, float (&o)[4]) {
+        const uint2 a = *reinterpret_cast<const uint2*>(p);
+        o[0] = Vec<__nv_bfloat16>::lo(a.x); o[1] = Vec<__nv_bfloat16>::hi(a.x);
+        o[2] = Vec<__nv_bfloat16>::lo(a.y); o[3] = Vec<__nv_bfloat16>::hi(a.y);
+    }
+    static __device__ __forceinline__ float2 ld2(const uint8_t* p) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        return make_float2(Vec<__nv_bfloat16>::lo(u), Vec<__nv_bfloat16>::hi(u));
+    }
 };
 
 template <typename T, int R, int MAXT>
@@ -231,8 +281,9 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                                                         const T* __restrict__ Cm, const float* __restrict__ lam,
                                                         const T* __restrict__ theta, const T* __restrict__ prev_B,
                                                         const T* __restrict__ prev_x, T* __restrict__ y) {
-    extern __shared__ __align__(16) float red[];   // [2][warps][R][P]
+    extern __shared__ __align__(16) float red[];   // [2][warps][R][P], then the staging area
     const int N = a.N, P = a.P, P4 = a.P4, H = a.H;
+    constexpr int es = sizeof(T);
     if ((int)blockDim.x != P4 * (N / kRPT)) {
         if (threadIdx.x == 0) m3::set_status(m3::kStatusBadLaunch);
         return;
@@ -244,41 +295,95 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
     const int n0 = g * kRPT, p0 = 4 * q;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
+    const int nthr = blockDim.x;
     float* st = state + unit * (int64_t)N * P + (int64_t)n0 * P + p0;
+    uint8_t* prev_slot = reinterpret_cast<uint8_t*>(red + 2 * nwarps * R * P);
+    uint8_t* bufs = prev_slot + a.xb + a.nb;
+    const int64_t ngroups = (a.k + kGroup - 1) / kGroup;
+    const bool has_theta = theta != nullptr;
+    const bool theta16 = ((N / 2) * es) % 16 == 0;
 
+    // token j's slot in the staging area
+    auto slot = [&](int64_t j) { return bufs + (size_t)((j / kGroup) % a.nbuf) * kGroup * a.tokb + (j % kGroup) * a.tokb; };
+    // issue the copies of group gi's tokens (every thread takes a share; lambda = NULL
+    // is written as 1 directly)
+    auto issue_group = [&](int64_t gi) {
+        const int64_t j0 = gi * kGroup;
+        const int nt = (int)((a.k - j0) < kGroup ? (a.k - j0) : kGroup);
+        const int cx = a.xb / 16, cn = (R * N * es) / 16;
+        const int ck = has_theta ? (theta16 ? ((N / 2) * es) / 16 : ((N / 2) * es) / 4) : 0;
+        const int per = cx + 2 * cn + ck + 2;
+        for (int e = threadIdx.x; e < nt * per; e += nthr) {
+            const int jj = e / per;
+            int c = e - jj * per;
+            const int64_t j = j0 + jj;
+            const int64_t tj = (b * a.k + j) * H + h;
+            uint8_t* d = slot(j);
+            if (c < cx) { ptx::cp_async16(d + c * 16, reinterpret_cast<const uint8_t*>(x + tj * R * P) + c * 16); continue; }
+            c -= cx;
+            if (c < cn) { ptx::cp_async16(d + a.xb + c * 16, reinterpret_cast<const uint8_t*>(Bm + tj * R * N) + c * 16); continue; }
+            c -= cn;
+            if (c < cn) { ptx::cp_async16(d + a.xb + a.nb + c * 16, reinterpret_cast<const uint8_t*>(Cm + tj * R * N) + c * 16); continue; }
+            c -= cn;
+            uint8_t* dk = d + a.xb + 2 * a.nb;
+            const uint8_t* sk = reinterpret_cast<const uint8_t*>(theta + tj * (N / 2));
+            if (c < ck) {
+                if (theta16) ptx::cp_async16(dk + c * 16, sk + c * 16);
+                else ptx::cp_async4(dk + c * 4, sk + c * 4, true);
+                continue;
+            }
+            c -= ck;
+            float* ds = reinterpret_cast<float*>(dk + a.kb);
+            if (c == 0) ptx::cp_async4(ds, dt + tj, true);
+            else if (lam) ptx::cp_async4(ds + 1, lam + tj, true);
+            else ds[1] = 1.0f;
+        }
+    };
+
+    // the caller's previous token and group 0, then the state (the bulk of the bytes)
+    const bool has_prev0 = prev_B != nullptr;
+    if (has_prev0) {
+        for (int c = threadIdx.x; c < a.xb / 16 + (R * N * es) / 16; c += nthr) {
+            if (c < a.xb / 16) ptx::cp_async16(prev_slot + c * 16, reinterpret_cast<const uint8_t*>(prev_x + unit * R * P) + c * 16);
+            else ptx::cp_async16(prev_slot + a.xb + (c - a.xb / 16) * 16,
+                                 reinterpret_cast<const uint8_t*>(prev_B + unit * R * N) + (c - a.xb / 16) * 16);
+        }
+    }
+    issue_group(0);
+    ptx::cp_async_commit();
     float4 hs[kRPT];
 #pragma unroll
     for (int i = 0; i < kRPT; ++i) hs[i] = __ldcs(reinterpret_cast<const float4*>(st + (int64_t)i * P));
     const float A_h = __ldg(A + h);
 
     for (int64_t j = 0; j < a.k; ++j) {
-        const int64_t tj = (b * a.k + j) * H + h;          // token j of this (b, h) in [b, k, h]
-        const float d = __ldg(dt + tj);
-        const float l = lam ? __ldg(lam + tj) : 1.0f;
+        if (j % kGroup == 0) {
+            ptx::cp_async_wait_all();   // this group's copies (the only ones in flight)
+            __syncthreads();
+        }
+        const uint8_t* cur = slot(j);
+        const bool has_prev = (j > 0) || has_prev0;
+        const uint8_t* prv = j > 0 ? slot(j - 1) : prev_slot;
+        const float* sc = reinterpret_cast<const float*>(cur + a.xb + 2 * a.nb + a.kb);
+        const float d = sc[0], l = sc[1];
         const float alpha = expf(d * A_h);
         const float beta = (1.0f - l) * d * alpha;
         const float gamma = l * d;
-        // the previous token's B and x: token j - 1 of this call, or the caller's
-        const bool has_prev = (j > 0) || (prev_B != nullptr);
-        const T* pxp = j > 0 ? x + (tj - H) * R * P : (has_prev ? prev_x + unit * R * P : nullptr);
-        const T* pBp = j > 0 ? Bm + (tj - H) * R * N + n0 : (has_prev ? prev_B + unit * R * N + n0 : nullptr);
         float xr[R][4], pxr[R][4];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            Vec<T>::ld4(x + (tj * R + r) * P + p0, xr[r]);
+            SVec<T>::ld4(cur + (r * P + p0) * es, xr[r]);
             if (has_prev) {
-                Vec<T>::ld4(pxp + r * P + p0, pxr[r]);
+                SVec<T>::ld4(prv + (r * P + p0) * es, pxr[r]);
             } else {
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) pxr[r][jj] = 0.0f;
             }
         }
-        const T* Bp = Bm + tj * R * N + n0;
-        const T* Cp = Cm + tj * R * N + n0;
         float cs[kRPT / 2], sn[kRPT / 2];
         {
             float th[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (theta) Vec<T>::ld4(theta + tj * (N / 2) + n0 / 2, th);
+            if (has_theta) SVec<T>::ld4(cur + a.xb + 2 * a.nb + (n0 / 2) * es, th);
 #pragma unroll
             for (int m = 0; m < kRPT / 2; ++m) __sincosf(reduce_2pi(th[m]), &sn[m], &cs[m]);
         }
@@ -294,9 +399,9 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
             float2 br[R], pbr[R], cr[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                br[r] = Vec<T>::ld2(Bp + r * N + 2 * m);
-                cr[r] = Vec<T>::ld2(Cp + r * N + 2 * m);
-                pbr[r] = has_prev ? Vec<T>::ld2(pBp + r * N + 2 * m) : make_float2(0.0f, 0.0f);
+                br[r] = SVec<T>::ld2(cur + a.xb + (r * N + n0 + 2 * m) * es);
+                cr[r] = SVec<T>::ld2(cur + a.xb + a.nb + (r * N + n0 + 2 * m) * es);
+                pbr[r] = has_prev ? SVec<T>::ld2(prv + a.xb + (r * N + n0 + 2 * m) * es) : make_float2(0.0f, 0.0f);
             }
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
@@ -333,7 +438,14 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                     make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < R * P; e += blockDim.x) {
+        // the first token of a group is done: every read of the group before it has
+        // happened, so the next group can land in that buffer
+        if (j % kGroup == 0 && j / kGroup + 1 < ngroups) {
+            issue_group(j / kGroup + 1);
+            ptx::cp_async_commit();
+        }
+        const int64_t tj = (b * a.k + j) * H + h;
+        for (int e = threadIdx.x; e < R * P; e += nthr) {
             float acc = 0.0f;
             for (int w = 0; w < nwarps; ++w) acc += rb[w * R * P + e];
             Vec<T>::st(y + tj * R * P + e, acc);

@@ -48,6 +48,10 @@ _lib.m3_scan_fwd_bcnorm.argtypes = [_dp] + [_vp] * 11 + [ctypes.c_float] + [_vp]
 _lib.m3_scan_fwd_bcnorm.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
+_lib.m3_scan_bwd_workspace_size.argtypes = [_dp]
+_lib.m3_scan_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.m3_scan_bwd.argtypes = [_dp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+_lib.m3_scan_bwd.restype = ctypes.c_int
 _lib.m3_step_k.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step_k.restype = ctypes.c_int
 _lib.m3_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _vp]
@@ -183,6 +187,33 @@ def m3_step(state, x_t, dt_t, A, B_t, C_t, lam_t, theta_t, prev_B, prev_x, y_t, 
                       _ptr(lam_t), _ptr(theta_t), _ptr(prev_B), _ptr(prev_x), _ptr(y_t), _stream(stream))
     if rc != M3_OK:
         raise M3Error(rc, "m3_step")
+
+
+def m3_scan_bwd_workspace_size(dims: m3_dims) -> int:
+    return int(_lib.m3_scan_bwd_workspace_size(ctypes.byref(dims)))
+
+
+def m3_scan_bwd(x, dt, A, B, C, lam, theta, dy, dfinal, dx, ddt, dA, dB, dC, dlam, dtheta, workspace,
+                workspace_bytes: int, chunk: int = 64, stream=None, dims: m3_dims | None = None) -> None:
+    """Backward pass of the prefill: writes dx, ddt, dA [h], dB, dC, dlam (if
+    lam is given) and dtheta (if theta is given) from the upstream dy and
+    dfinal (or None).  workspace: a device buffer of at least
+    m3_scan_bwd_workspace_size(dims) bytes.  Raises M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, chunk)
+    rc = _lib.m3_scan_bwd(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam), _ptr(theta),
+                          _ptr(dy), _ptr(dfinal), _ptr(dx), _ptr(ddt), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dlam),
+                          _ptr(dtheta), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_scan_bwd")
+
+
+def raw_scan_bwd(dims: m3_dims, ptrs, stream=None) -> int:
+    """Direct call with raw addresses (x, dt, A, B, C, lam, theta, dy, dfinal, dx,
+    ddt, dA, dB, dC, dlam, dtheta, workspace, workspace_bytes); returns the
+    status code."""
+    *p, ws_bytes = ptrs
+    return int(_lib.m3_scan_bwd(ctypes.byref(dims), *p, int(ws_bytes), stream))
 
 
 def m3_step_k(state, x, dt, A, B, C, lam, theta, prev_B, prev_x, y, stream=None,

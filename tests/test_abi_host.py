@@ -32,7 +32,8 @@ def declared_symbols():
 
 def test_every_declared_symbol_is_exported(m3):
     names = declared_symbols()
-    assert {"m3_scan_fwd", "m3_step", "m3_step_k", "m3_scan_workspace_size", "m3_status_string"} <= set(names)
+    assert {"m3_scan_fwd", "m3_scan_bwd", "m3_step", "m3_step_k", "m3_scan_workspace_size",
+            "m3_status_string"} <= set(names)
     lib = ctypes.CDLL(m3.LIBRARY_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -189,3 +190,32 @@ def test_step_k_validation(m3):
     # no token or no batch row: nothing to do, nothing launched
     assert m3.raw_step_k(_dims(m3, seqlen=0), _step_ptrs()) == m3.M3_OK
     assert m3.raw_step_k(_dims(m3, seqlen=8, batch=0), _step_ptrs()) == m3.M3_OK
+
+
+def _bwd_ptrs(**over):
+    names = ("x", "dt", "A", "B", "C", "lam", "theta", "dy", "dfinal", "dx", "ddt", "dA", "dB", "dC", "dlam",
+             "dtheta", "ws", "wsb")
+    p = {k: FAKE for k in names}
+    p.update(wsb=1 << 40)
+    p.update(over)
+    return [p[k] for k in names]
+
+
+def test_bwd_validation(m3):
+    d = _dims(m3)
+    need = m3.m3_scan_bwd_workspace_size(d)
+    # chunk states of every (b, h): (ceil(100 / 64) + 1) x 64 x 64 fp32 each, and more
+    assert need >= 2 * 4 * 3 * 64 * 64 * 4
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(dx=None)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(dA=None)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(dlam=None)) == m3.M3_ERR_NULL        # lambda given, no dlambda
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(dtheta=None)) == m3.M3_ERR_NULL      # theta given, no dtheta
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(dx=FAKE + 1)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(ws=None)) == m3.M3_ERR_WORKSPACE
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(wsb=need - 1)) == m3.M3_ERR_WORKSPACE
+    assert m3.raw_scan_bwd(d, _bwd_ptrs(ws=FAKE + 16)) == m3.M3_ERR_ALIGN    # workspace: 256-byte aligned
+    # more than 64 rows per chunk is not taken (nor a workspace size given for it)
+    assert m3.raw_scan_bwd(_dims(m3, chunk=128), _bwd_ptrs()) == m3.M3_ERR_UNSUPPORTED
+    assert m3.raw_scan_bwd(_dims(m3, rank=2, chunk=64), _bwd_ptrs()) == m3.M3_ERR_UNSUPPORTED
+    assert m3.m3_scan_bwd_workspace_size(_dims(m3, chunk=128)) == 0
+    assert m3.raw_scan_bwd(_dims(m3, dstate=7), _bwd_ptrs()) == m3.M3_ERR_SHAPE
