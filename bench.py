@@ -378,6 +378,59 @@ def time_prefill(m3, stream, shape, seed, dev, steps, warmup, bcnorm=False):
     return ms
 
 
+def bwd_bytes(shape: inputs.ScanShape) -> int:
+    """Algorithmic bytes of one backward pass: the forward's inputs, dy and
+    dfinal read once; dx, ddt, dA, dB, dC, dlambda, dtheta written once (the
+    workspace of chunk states excluded)."""
+    b, T, H, P, N, R = shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.rank
+    es = 2 if shape.dtype == "bf16" else 4
+    tok = b * T * H
+    per_tok = R * P * es * 2 + R * N * es * 2 + 4 + (4 if shape.with_lambda else 0) + \
+        ((N // 2) * es if shape.with_theta else 0)
+    n = tok * per_tok * 2           # inputs and their gradients
+    n += tok * R * P * es           # dy
+    n += b * H * N * P * 4          # dfinal
+    n += H * 4 * 2                  # A, dA
+    return n
+
+
+def time_bwd(m3, stream, shape, seed, dev, steps, warmup):
+    """Device time (ms) of one m3_scan_bwd of `shape` on resident inputs (CUDA
+    events on `stream`), with its workspace bytes."""
+    inp = inputs.make_scan_inputs(shape, seed)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    g = torch.Generator(device="cpu").manual_seed(seed + 1)
+    b, T, H, R, P = d["x"].shape
+    N = d["B"].shape[-1]
+    dy = torch.randn(b, T, H, R, P, generator=g).to(d["x"].dtype).to(dev)
+    dfinal = torch.randn(b, H, N, P, generator=g).to(dev)
+    dims = m3.scan_dims(d["x"], d["B"], shape.chunk)
+    wsb = m3.m3_scan_bwd_workspace_size(dims)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    out = [torch.empty_like(d["x"]), torch.empty_like(d["dt"]), torch.empty_like(d["A"]), torch.empty_like(d["B"]),
+           torch.empty_like(d["C"]), torch.empty_like(d["dt"]) if d["lam"] is not None else None,
+           torch.empty_like(d["theta"]) if d["theta"] is not None else None]
+
+    def launch():
+        m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], dy, dfinal, *out, ws, wsb,
+                       stream=stream, dims=dims)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            launch()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if m3.m3_device_status(stream) != m3.M3_OK:
+        raise RuntimeError("device status set during the backward")
+    ms = e0.elapsed_time(e1) / steps
+    del d, dy, dfinal, ws, out
+    torch.cuda.empty_cache()
+    return ms, wsb
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -397,6 +450,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen (profiling captures)")
     ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward pass")
     ap.add_argument("--decode-only", action="store_true", help="only the decode sweep (profiling captures)")
     args = ap.parse_args()
 
@@ -546,6 +600,17 @@ def main():
             "GB_per_s": wb / (wms * 1e-3) / 1e9, "hbm_frac": wb / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": wb}
         result["other_prefill"] = other
+
+    if not args.no_bwd and rank == 0:
+        # the backward pass of the timed workload (training): m3_scan_bwd
+        bms, wsb = time_bwd(m3, stream, shape, args.workload, dev, steps=10, warmup=3)
+        bb = bwd_bytes(shape)
+        result["backward"] = {
+            "workload": cfg_name, "entry": "m3_scan_bwd", "ms_per_step": bms,
+            "tokens_per_s": shape.batch * shape.seqlen / (bms * 1e-3), "GB_per_s": bb / (bms * 1e-3) / 1e9,
+            "hbm_frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": bb,
+            "workspace_bytes": wsb, "launches_per_step": 3,
+            "vs_forward": bms / ms}
 
     if not args.no_decode and rank == 0:
         dec = {}
