@@ -227,6 +227,30 @@ M3_API int m3_scan_bwd(const m3_dims* d, const void* x, const float* dt, const f
                        void* dB, void* dC, float* dlambda, void* dtheta, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* m3_scan_bwd for callers that cannot allocate device memory -- a host whose
+ * allocator belongs to another runtime or framework, a process held to a fixed
+ * memory budget, or code that must not call the allocator inside a serving
+ * loop.  The pages have no counterpart: this is an interface choice.  Same
+ * arguments and result as m3_scan_bwd, without the workspace: the scratch is a
+ * fixed 32 MiB array inside the library's device image, present on every GPU
+ * that loads the library until the process exits.
+ *   - Sizes whose workspace (m3_scan_bwd_workspace_size) exceeds 32 MiB are
+ *     rejected with M3_ERR_WORKSPACE before anything runs.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array.  Calls whose work overlaps
+ *     on the GPU (other streams, other host threads) race on it and corrupt
+ *     each other's result: order them on one stream or synchronise.  No part of
+ *     the array needs to start at zero (every byte a call reads it wrote
+ *     first), so the previous call's contents do no harm.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine. */
+M3_API int m3_scan_bwd_noalloc(const m3_dims* d, const void* x, const float* dt, const float* A,
+                               const void* B, const void* C, const float* lambda, const void* theta,
+                               const void* dy, const float* dfinal, void* dx, float* ddt, float* dA,
+                               void* dB, void* dC, float* dlambda, void* dtheta, void* stream);
+
 /* k decode steps in one launch (multi-token / speculative decode): the same
  * recurrence over k = d->seqlen consecutive tokens of every (b, h), reading
  * and writing the state once instead of k times (Mamba-3 summary page §3.3:

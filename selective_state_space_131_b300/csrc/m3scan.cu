@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "m3scan.h"
 #include "common.cuh"
@@ -477,6 +478,64 @@ int m3_step_k(const m3_dims* d, float* state, const void* x, const float* dt, co
     dc.chunk = (16 * d->rank == m3ws::kRows) ? 32 : 16;
     return m3_scan_fwd_from(&dc, x, dt, A, B, C, lambda, theta, state, prev_B, prev_x, y, state, nullptr, 0,
                             stream);
+}
+
+// ---------------------------------------------------------------------------
+// Backward pass without caller-provided workspace, for callers that cannot
+// allocate device memory (a host whose allocator belongs to another runtime or
+// framework, a process running under a fixed memory budget, code that must not
+// touch the allocator inside a serving loop).  Its scratch is one fixed array in
+// this library's device image: every GPU that loads the library holds it until
+// the process exits.
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
+static __device__ __align__(256) uint8_t g_bwd_scratch[kNoAllocScratchBytes];
+
+// The device address of g_bwd_scratch, looked up once per device with that
+// device current (in host code the array's name is a host-side stand-in, not a
+// device address).
+constexpr int kMaxScratchDevices = 256;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxScratchDevices];
+
+int scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return M3_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxScratchDevices) return M3_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return M3_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return M3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int m3_scan_bwd_noalloc(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B,
+                        const void* C, const float* lambda, const void* theta, const void* dy, const float* dfinal,
+                        void* dx, float* ddt, float* dA, void* dB, void* dC, float* dlambda, void* dtheta,
+                        void* stream) {
+    const int rc = check_dims(d, true);
+    if (rc != M3_OK) return rc;
+    const bool has_tokens = d->batch > 0 && d->seqlen > 0;
+    if (has_tokens && bwd_supported(d) &&
+        m3bwd::work_bytes(d->batch * d->heads, bwd_geo(d)) > kNoAllocScratchBytes)
+        return M3_ERR_WORKSPACE;   // these sizes need more than the fixed scratch holds
+    void* scratch = nullptr;
+    if (has_tokens) {
+        const int src = scratch_address(&scratch);
+        if (src != M3_OK) return src;
+    }
+    return m3_scan_bwd(d, x, dt, A, B, C, lambda, theta, dy, dfinal, dx, ddt, dA, dB, dC, dlambda, dtheta, scratch,
+                       has_tokens ? kNoAllocScratchBytes : 0, stream);
 }
 
 int m3_device_status(void* stream) {

@@ -52,6 +52,8 @@ _lib.m3_scan_bwd_workspace_size.argtypes = [_dp]
 _lib.m3_scan_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.m3_scan_bwd.argtypes = [_dp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_bwd.restype = ctypes.c_int
+_lib.m3_scan_bwd_noalloc.argtypes = [_dp] + [_vp] * 16 + [_vp]
+_lib.m3_scan_bwd_noalloc.restype = ctypes.c_int
 _lib.m3_step_k.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step_k.restype = ctypes.c_int
 _lib.m3_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _vp]
@@ -214,6 +216,21 @@ def raw_scan_bwd(dims: m3_dims, ptrs, stream=None) -> int:
     status code."""
     *p, ws_bytes = ptrs
     return int(_lib.m3_scan_bwd(ctypes.byref(dims), *p, int(ws_bytes), stream))
+
+
+def m3_scan_bwd_noalloc(x, dt, A, B, C, lam, theta, dy, dfinal, dx, ddt, dA, dB, dC, dlam, dtheta,
+                        chunk: int = 64, stream=None, dims: m3_dims | None = None) -> None:
+    """m3_scan_bwd without a workspace argument, for callers that cannot
+    allocate device memory: the library's fixed 32 MiB scratch serves instead
+    (sizes needing more raise M3Error with M3_ERR_WORKSPACE; calls that overlap
+    on the GPU share that scratch and must be ordered).  Raises M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, chunk)
+    rc = _lib.m3_scan_bwd_noalloc(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam),
+                                  _ptr(theta), _ptr(dy), _ptr(dfinal), _ptr(dx), _ptr(ddt), _ptr(dA), _ptr(dB),
+                                  _ptr(dC), _ptr(dlam), _ptr(dtheta), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_scan_bwd_noalloc")
 
 
 def m3_step_k(state, x, dt, A, B, C, lam, theta, prev_B, prev_x, y, stream=None,
