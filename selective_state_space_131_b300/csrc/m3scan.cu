@@ -15,6 +15,7 @@
 #include "scan_ws.cuh"
 #include "scan_chunk.cuh"
 #include "scan_bwd.cuh"
+#include "scan_bwd_tc.cuh"
 #include "selftest.cuh"
 
 namespace {
@@ -246,6 +247,86 @@ bool bwd_supported(const m3_dims* d) {
     return (size_t)g.bytes <= kMaxSmem && (size_t)g.c_bytes <= kMaxSmem;
 }
 
+// The tensor-core backward: bf16, N = P = 64, R in {1, 2, 4}, one 64-row tile per
+// chunk, every tensor the TMA reads or writes 16-byte aligned.
+bool bwd_tc_shape(const m3_dims* d, const void* const* ptrs, int n) {
+    if (!m3ws::supports(*d) || d->dstate != 64 || d->chunk * d->rank != m3ws::kRows) return false;
+    for (int i = 0; i < n; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i])) return false;
+    return true;
+}
+
+// 4-D map over theta [b, T, h, K] bf16, box (K, 1, Q, 1), no swizzle: the tile
+// lands as [Q][K] rows of 2 K bytes.
+bool make_map_theta_plain(CUtensorMap* m, const void* base, const m3_dims& d, int Q) {
+    const cuuint64_t K = (cuuint64_t)d.dstate / 2;
+    cuuint64_t dims[4] = {K, (cuuint64_t)d.heads, (cuuint64_t)d.seqlen, (cuuint64_t)d.batch};
+    cuuint64_t strides[3] = {K * 2, (cuuint64_t)d.heads * K * 2, (cuuint64_t)d.seqlen * d.heads * K * 2};
+    cuuint32_t box[4] = {(cuuint32_t)K, 1, (cuuint32_t)Q, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return m3ws::encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                  const float* lam, const void* theta, const void* dy, const float* dfinal, void* dx, float* ddt,
+                  float* dA, void* dB, void* dC, float* dlam, void* dtheta, const m3bwd::Work& w, cudaStream_t s) {
+    // pass 1: the forward tensor-core kernel with chunk checkpoints (its y goes
+    // to dx, which pass 2 overwrites)
+    int rc = m3ws::launch(*d, x, dt, A, B, C, lam, theta, nullptr, nullptr, nullptr, dx, nullptr, s, nullptr,
+                          nullptr, nullptr, nullptr, 0.0f, w.G, w.phi);
+    if (rc != M3_OK) return rc;
+    // pass 2
+    const int Q = m3ws::kRows / (int)d->rank;
+    CUtensorMap maps[5];
+    memset(maps, 0, sizeof(maps));
+    if (!m3ws::make_map5(&maps[0], x, *d, 64, Q) || !m3ws::make_map5(&maps[1], B, *d, 64, Q) ||
+        !m3ws::make_map5(&maps[2], C, *d, 64, Q) || !m3ws::make_map5(&maps[3], dy, *d, 64, Q))
+        return M3_ERR_CUDA;
+    if (theta) {
+        if (!make_map_theta_plain(&maps[4], theta, *d, Q)) return M3_ERR_CUDA;
+    } else {
+        maps[4] = maps[0];   // never read
+    }
+    m3bwdtc::Params prm;
+    prm.T = d->seqlen;
+    prm.H = (int)d->heads;
+    prm.nch = (int)((d->seqlen + Q - 1) / Q);
+    prm.dt = dt;
+    prm.A = A;
+    prm.lam = lam;
+    prm.theta = static_cast<const __nv_bfloat16*>(theta);
+    prm.dfinal = dfinal;
+    prm.ck_G = w.G;
+    prm.ck_phi = w.phi;
+    prm.dA_part = w.dA;
+    prm.dx = static_cast<__nv_bfloat16*>(dx);
+    prm.ddt = ddt;
+    prm.dB = static_cast<__nv_bfloat16*>(dB);
+    prm.dC = static_cast<__nv_bfloat16*>(dC);
+    prm.dlam = dlam;
+    prm.dtheta = static_cast<__nv_bfloat16*>(dtheta);
+    const unsigned grid = (unsigned)(d->batch * d->heads);
+#define M3_BWD_TC(RR)                                                                                           \
+    {                                                                                                          \
+        auto k = m3bwdtc::m3_bwd_tc_kernel<RR>;                                                                \
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, m3bwdtc::SMEM_BYTES) !=       \
+            cudaSuccess)                                                                                       \
+            return M3_ERR_CUDA;                                                                                \
+        k<<<grid, m3bwdtc::kThreads, m3bwdtc::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm); \
+    }
+    switch (d->rank) {
+        case 1: M3_BWD_TC(1); break;
+        case 2: M3_BWD_TC(2); break;
+        case 4: M3_BWD_TC(4); break;
+        default: return M3_ERR_UNSUPPORTED;
+    }
+#undef M3_BWD_TC
+    m3bwd::m3_bwd_dA_kernel<<<(unsigned)((d->heads + 127) / 128), 128, 0, s>>>(w.dA, d->batch, (int)d->heads, dA);
+    return launch_status();
+}
+
 template <typename T>
 int launch_bwd(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
                const float* lam, const void* theta, const void* dy, const float* dfinal, void* dx, float* ddt,
@@ -253,6 +334,11 @@ int launch_bwd(const m3_dims* d, const void* x, const float* dt, const float* A,
     const m3bwd::Geo g = bwd_geo(d);
     const int64_t units = d->batch * d->heads;
     const m3bwd::Work w = m3bwd::work_split(ws, units, g);
+    if constexpr (sizeof(T) == 2) {
+        const void* tma_ptrs[] = {x, B, C, theta, dy, dx, dB, dC};
+        if (bwd_tc_shape(d, tma_ptrs, 8))
+            return launch_bwd_tc(d, x, dt, A, B, C, lam, theta, dy, dfinal, dx, ddt, dA, dB, dC, dlam, dtheta, w, s);
+    }
     auto k1 = m3bwd::m3_bwd_ckpt_kernel<T>;
     auto k2 = m3bwd::m3_bwd_chunk_kernel<T>;
     int rc = prepare(k1, (size_t)g.c_bytes);

@@ -142,6 +142,11 @@ struct Params {
     const float* norm_bB;
     const float* norm_bC;
     float norm_eps;
+    // chunk checkpoints for the backward pass (CKPT variants only): the fp32 state
+    // G_{c-1} at the start of every chunk c and G_last, [b h][nch + 1][N][P], and
+    // the angle carry (reduced mod 2 pi) at the same points, [b h][nch + 1][K]
+    float* ck_G;
+    float* ck_phi;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -192,7 +197,7 @@ __device__ __forceinline__ uint32_t swz(int row, int g) {
     return (uint32_t)(row * 128 + (((g & 7) ^ (row & 7)) << 4) + (g >> 3) * (kRows * 128));
 }
 
-template <int NSLAB, int R, bool ROT, bool NORM>
+template <int NSLAB, int R, bool ROT, bool NORM, bool CKPT = false>
 __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     m3_scan_ws_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_B,
                       const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_th,
@@ -528,6 +533,14 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 __syncwarp();   // tcgen05.ld below is warp-aligned
                 ptx::tc_fence_after();
                 const float* cin = carry_buf + s * K + hf * PH;
+                if constexpr (CKPT) {
+                    // the angle before chunk c's first token, for the backward pass
+                    if (row == 0) {
+                        float* dst = prm.ck_phi + ((int64_t)unit * (nch + 1) + c) * K + hf * PH;
+#pragma unroll
+                        for (int q = 0; q < PH; ++q) dst[q] = cin[q];
+                    }
+                }
                 float* cout = carry_buf + (s ^ 1) * K + hf * PH;
                 const uint32_t taddr = tm_sy + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
@@ -822,6 +835,13 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 }
             }
             // (3) G_c = exp(cs_end) G_{c-1} + dG_c (fp32)
+            if constexpr (CKPT) {
+                // G_{c-1} for the backward pass (rows and columns as held here)
+                float* dst = prm.ck_G + (((int64_t)unit * (nch + 1) + c) * N + g_row) * kP + ((N == 64) ? hc * 32 : 0);
+#pragma unroll
+                for (int p4 = 0; p4 < GC / 4; ++p4)
+                    *reinterpret_cast<float4*>(dst + 4 * p4) = make_float4(G[4 * p4], G[4 * p4 + 1], G[4 * p4 + 2], G[4 * p4 + 3]);
+            }
             __syncwarp();
             {
                 const float dec = sc[CF::SC_DEC];
@@ -949,6 +969,19 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     // makes it visible.  A stop anywhere (abort_s) skips the write.
     __syncthreads();
     aborted = (abort_s != 0);
+    if constexpr (CKPT) {
+        // G_last and the final angle, after the last chunk (slot nch)
+        if (!aborted && tid >= kWG) {
+            const int w1 = warp - 4;
+            const int g_row = (N == 64) ? (w1 * 16 + (lane & 15)) : (w1 * 32 + lane);
+            float* dst = prm.ck_G + (((int64_t)unit * (nch + 1) + nch) * N + g_row) * kP + ((N == 64) ? (lane >> 4) * 32 : 0);
+#pragma unroll
+            for (int p4 = 0; p4 < GC / 4; ++p4)
+                *reinterpret_cast<float4*>(dst + 4 * p4) = make_float4(G[4 * p4], G[4 * p4 + 1], G[4 * p4 + 2], G[4 * p4 + 3]);
+        }
+        if (!aborted && tid < K)
+            prm.ck_phi[((int64_t)unit * (nch + 1) + nch) * K + tid] = ROT ? s_carry[(nch & 1) * K + tid] : 0.0f;
+    }
     if (!aborted && prm.final_state && tid >= kWG) {
         const int w1 = warp - 4;
         const int g_row = (N == 64) ? (w1 * 16 + (lane & 15)) : (w1 * 32 + lane);
@@ -1053,10 +1086,10 @@ inline bool make_map_theta(CUtensorMap* m, const void* base, const m3_dims& d, i
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NSLAB, int R, bool ROT, bool NORM>
+template <int NSLAB, int R, bool ROT, bool NORM, bool CKPT = false>
 int launch_cfg(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cudaStream_t s) {
     using CF = Cfg<NSLAB, R, ROT, NORM>;
-    auto k = m3_scan_ws_kernel<NSLAB, R, ROT, NORM>;
+    auto k = m3_scan_ws_kernel<NSLAB, R, ROT, NORM, CKPT>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return M3_ERR_CUDA;
     k<<<(unsigned)(d.batch * d.heads), kThreads, CF::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
@@ -1064,12 +1097,12 @@ int launch_cfg(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cud
     return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
-template <int NSLAB, bool ROT, bool NORM>
+template <int NSLAB, bool ROT, bool NORM, bool CKPT = false>
 int launch_r(const m3_dims& d, const CUtensorMap* maps, const Params& prm, cudaStream_t s) {
     switch (d.rank) {
-        case 1: return launch_cfg<NSLAB, 1, ROT, NORM>(d, maps, prm, s);
-        case 2: return launch_cfg<NSLAB, 2, ROT, NORM>(d, maps, prm, s);
-        case 4: return launch_cfg<NSLAB, 4, ROT, NORM>(d, maps, prm, s);
+        case 1: return launch_cfg<NSLAB, 1, ROT, NORM, CKPT>(d, maps, prm, s);
+        case 2: return launch_cfg<NSLAB, 2, ROT, NORM, CKPT>(d, maps, prm, s);
+        case 4: return launch_cfg<NSLAB, 4, ROT, NORM, CKPT>(d, maps, prm, s);
     }
     return M3_ERR_UNSUPPORTED;
 }
@@ -1083,7 +1116,7 @@ inline int launch(const m3_dims& d, const void* x, const float* dt, const float*
                   const float* lam, const void* theta, const float* h0, const void* prev_B, const void* prev_x,
                   void* y, float* final_state, cudaStream_t s, const float* norm_wB = nullptr,
                   const float* norm_wC = nullptr, const float* norm_bB = nullptr, const float* norm_bC = nullptr,
-                  float norm_eps = 0.0f) {
+                  float norm_eps = 0.0f, float* ck_G = nullptr, float* ck_phi = nullptr) {
     if (!supports(d)) return M3_ERR_UNSUPPORTED;
     const void* tma_ptrs[] = {x, B, C, theta, y};
     for (const void* p : tma_ptrs)
@@ -1114,7 +1147,14 @@ inline int launch(const m3_dims& d, const void* x, const float* dt, const float*
     prm.norm_bB = norm_bB;
     prm.norm_bC = norm_bC;
     prm.norm_eps = norm_eps;
+    prm.ck_G = ck_G;
+    prm.ck_phi = ck_phi;
     const bool norm = norm_wB != nullptr;
+    if (ck_G) {
+        // the checkpointing forward of the backward pass: N = 64, no normalisation
+        if (d.dstate != 64 || norm) return M3_ERR_UNSUPPORTED;
+        return rot ? launch_r<1, true, false, true>(d, maps, prm, s) : launch_r<1, false, false, true>(d, maps, prm, s);
+    }
     if (d.dstate == 64)
         return norm ? launch_n<1, true>(d, maps, prm, rot, s) : launch_n<1, false>(d, maps, prm, rot, s);
     return norm ? launch_n<2, true>(d, maps, prm, rot, s) : launch_n<2, false>(d, maps, prm, rot, s);
