@@ -85,7 +85,8 @@ def scan_bytes(shape: inputs.ScanShape) -> int:
 
 
 def scan_flops(shape: inputs.ScanShape) -> int:
-    """The chunked algorithm's flop count per token and head, R [2Q(N+P) + 4NP]."""
+    """The chunked algorithm's flop count per token and head, R [2Q(N+P) + 4NP],
+    at the chunk Q the kernel executes (shape.chunk)."""
     b, T, H, P, N, R, Q = (shape.batch, shape.seqlen, shape.heads, shape.headdim, shape.dstate, shape.rank,
                            shape.chunk)
     return b * T * H * R * (2 * Q * (N + P) + 4 * N * P)
@@ -585,12 +586,22 @@ def main():
             if w == args.workload:
                 continue
             sh = inputs.CONFIGS[w]
+            note = None
+            if sh.chunk * sh.rank != 64:
+                # the tensor-core kernel's chunk is one 64-row tile: 64 / R tokens (16 at
+                # R = 4); the workload's own chunk runs on the chunked CUDA-core kernel
+                note = (f"chunk {64 // sh.rank} executed (the 64-row tensor-core tile at R = {sh.rank}); "
+                        f"chunk {sh.chunk} runs on the CUDA-core chunked kernel")
+                sh = inputs.ScanShape(**{**sh.__dict__, "chunk": 64 // sh.rank})
             wms = time_prefill(m3, stream, sh, w, dev, steps=20, warmup=3)
             wb = scan_bytes(sh)
             other[inputs.CONFIG_NAMES[w]] = {
                 "ms_per_step": wms, "tokens_per_s": sh.batch * sh.seqlen / (wms * 1e-3),
                 "GB_per_s": wb / (wms * 1e-3) / 1e9, "hbm_frac": wb / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                "algorithmic_bytes": wb, "tensor_tflops": scan_flops(sh) / (wms * 1e-3) / 1e12}
+                "algorithmic_bytes": wb, "chunk": sh.chunk,
+                "tensor_tflops": scan_flops(sh) / (wms * 1e-3) / 1e12}
+            if note:
+                other[inputs.CONFIG_NAMES[w]]["note"] = note
         # the timed workload again with the B / C normalisation and biases fused
         # into the prologue (m3_scan_fwd_bcnorm; the parameters add 1 KB per head)
         wms = time_prefill(m3, stream, shape, args.workload, dev, steps=20, warmup=3, bcnorm=True)

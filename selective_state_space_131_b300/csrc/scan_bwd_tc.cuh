@@ -64,8 +64,10 @@ constexpr int F_DPHI = F_PEND + 4;                                              
 constexpr int F_PHI0 = F_DPHI + 32;                                                      // [32] angle at chunk start
 constexpr int F_DTOK = F_PHI0 + 32;                                                      // [2][64] ddt, dlam of the chunk
 constexpr int F_CZM = F_DTOK + 128, F_CZE = F_CZM + 64;                                  // per column
-constexpr int F_END = F_CZE + 64;
-constexpr int SMEM_BYTES = OFF_F + F_END * 4 + 1024;
+constexpr int F_SEG = F_CZE + 64;                                                        // [4][32] segment totals
+constexpr int F_END = F_SEG + 128;
+constexpr int OFF_GB = (OFF_F + F_END * 4 + 1023) & ~1023;   // fp32 G checkpoint, 2 stages x [64][64]
+constexpr int SMEM_BYTES = OFF_GB + 2 * 64 * 64 * 4 + 1024;
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_DSP = 64, TM_T2 = 128, TM_XG = 192, TM_DX = 256, TM_DC = 320, TM_DB = 384,
                    TM_DGU = 448, TM_COLS = 512;
@@ -185,6 +187,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_5d(base + ST_DY, &map_dy, &bar_ld[st], 0, 0, h, t0, b);
         if (rot) ptx::tma_load_4d(base + ST_TH, &map_th, &bar_ld[st], 0, h, t0, b);
     };
+    // warpgroup 0: each thread copies its own slice (row `row`, columns 32 hc ..) of
+    // checkpoint slot c into stage st of the fp32 buffer (it alone reads it back)
+    auto issue_ckpt = [&](int c, int st) {
+        const float* src = prm.ck_G + (((int64_t)unit * (prm.nch + 1) + c) * 64 + row) * 64 + 32 * hc;
+        float* dst = reinterpret_cast<float*>(smem + OFF_GB) + st * 4096 + row * 64 + 32 * hc;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ptx::cp_async16(dst + 4 * q, src + 4 * q);
+        ptx::cp_async_commit();
+    };
+    // warps 6 and 7: dtheta of chunk cc from its rows' dPhi (F_DPR), suffix sums in
+    // two segments of Q / 2 tokens per pair, carried from the chunks after it
+    auto dtheta_chunk = [&](int cc) {
+        const int seg = warp - 6;
+        constexpr int QS = Q / 2;
+        const int64_t tc0 = (int64_t)cc * Q;
+        const int ntc = (int)((T - tc0) < Q ? (T - tc0) : Q);
+        float v[QS];
+        float tot = 0.0f;
+#pragma unroll
+        for (int q = 0; q < QS; ++q) {
+            const int t = seg * QS + q;
+            float a = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) a += F[F_DPR + (t * R + r) * K + lane];
+            v[q] = a;
+            tot += a;
+        }
+        F[F_SEG + seg * 32 + lane] = tot;
+        ptx::bar_sync(3, 64);
+        float acc = F[F_DPHI + lane] + (seg == 0 ? F[F_SEG + 32 + lane] : 0.0f);
+#pragma unroll
+        for (int q = QS - 1; q >= 0; --q) {
+            const int t = seg * QS + q;
+            acc += v[q];
+            if (t < ntc) prm.dtheta[(((int64_t)b * T + tc0 + t) * prm.H + h) * K + lane] = __float2bfloat16_rn(acc);
+        }
+        ptx::bar_sync(3, 64);
+        if (seg == 0) F[F_DPHI + lane] = acc;
+    };
     auto issue_scalars = [&](int c, int st) {
         float* dst = F + F_DL + st * 2 * 68;
         for (int tt = lane; tt <= Q; tt += 32) {
@@ -235,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     if (tid == 32) issue_loads(nch - 1, (nch - 1) & 1);
-    if (warp == 2) issue_scalars(nch - 1, (nch - 1) & 1);
+    if (warp == 7) issue_scalars(nch - 1, (nch - 1) & 1);
+    if (wg == 0) issue_ckpt(nch - 1, (nch - 1) & 1);
     bool fail = false;
     float dA_acc = 0.0f;
 
@@ -247,16 +289,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next chunk (in reverse) into the other stage, free since the
         // previous iteration's batch 2 completed
         if (c > 0 && tid == 32) issue_loads(c - 1, st ^ 1);
-        // ---- (1) checkpoint G_{c-1} (warpgroup 0: fp32 slice for <dG, G>, bf16 tile),
-        //      angle at chunk start; scalars (warp 4); angles (warp 5)
-        float gsl[32];
+        // ---- (1) checkpoint G_{c-1} (warpgroup 0: fp32 slice for <dG, G>, bf16 tile;
+        //      the next chunk's slice prefetched); dt / lambda (warp 7)
         if (wg == 0) {
-            const float* src = prm.ck_G + ((ckb + c) * 64 + row) * 64 + 32 * hc;
+            ptx::cp_async_wait_all();   // this thread's slice of slot c
+            float gsl[32];
+            const float* src = reinterpret_cast<const float*>(smem + OFF_GB) + st * 4096 + row * 64 + 32 * hc;
 #pragma unroll
             for (int p4 = 0; p4 < 8; ++p4) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(src) + p4);
+                const float4 v = *reinterpret_cast<const float4*>(src + 4 * p4);
                 gsl[4 * p4] = v.x; gsl[4 * p4 + 1] = v.y; gsl[4 * p4 + 2] = v.z; gsl[4 * p4 + 3] = v.w;
             }
+            if (c > 0) issue_ckpt(c - 1, st ^ 1);
             tile_put32(smem + OFF_G, row, hc, gsl);
             float part = 0.0f;
 #pragma unroll
@@ -265,13 +309,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             if (lane == 0) F[F_RED + wq] = part;
         }
-        if (warp == 2) {
+        if (warp == 7) {
             ptx::cp_async_wait_all();   // this chunk's dt / lambda
             __syncwarp();
             if (c > 0) issue_scalars(c - 1, st ^ 1);
         }
+        float phi0 = 0.0f;   // warpgroup 1: the angle of pair `lane` before the chunk
+        if (wg == 1 && prm.theta) phi0 = __ldg(prm.ck_phi + (ckb + c) * K + lane);
+        ptx::fence_proxy_async_smem();   // the G tile, for the MMAs below
+        ptx::tc_fence_before();
         __syncthreads();
-        if (warp == 4) {
+        ptx::tc_fence_after();
+        if (tid == 32) {
+            // the products that need neither the rotation nor the mask, as soon as the
+            // tiles are in: dS' = dY X^T, T2 = dY G^T, XG = X dG^T
+            if (!ptx::mbar_wait(&bar_ld[st], ((nch - 1 - c) >> 1) & 1, kWaitBudget)) {
+                m3::set_status(m3::kStatusWaitTimeout);
+                abort_s = 1;
+            } else {
+                ptx::tc_fence_after();
+                const uint32_t x_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_X), 16);
+                const uint32_t y_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_DY), 16);
+                const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_G), 16);
+                const uint32_t d_lo = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DG), 16);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {   // K-major operands: 16 columns = +32 bytes
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DSP, y_lo + 2 * k, x_lo + 2 * k, kIdKK, k > 0);
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_T2, y_lo + 2 * k, g_lo + 2 * k, kIdKK, k > 0);
+                    ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_XG, x_lo + 2 * k, d_lo + 2 * k, kIdKK, k > 0);
+                }
+            }
+        }
+        __syncwarp();   // warp 1 reconverges before its other lanes wait: a lane parked in
+                        // mbarrier.try_wait can hold back the issuing lane of its warp
+        if (warp == 0) {
             // chunk-local cs (log2 units), gamma, w, s = 2^(cs_end - cs) w, exp(cs)
             const float* sdt = F + F_DL + st * 2 * 68;
             const float* slm = sdt + 68;
@@ -309,19 +380,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (warp == 5 && prm.theta) {
-            // the cumulative angle of every token and pair (lane = pair), fp32 from
-            // the checkpointed angle at the chunk start
+        if (wg == 1 && prm.theta) {
+            // the cumulative angle of every token and pair: 4 segments of Q / 4 tokens
+            // per pair (warp 4 + seg), fp32 from the checkpointed angle at the chunk start
+            const int seg = warp - 4;
+            constexpr int QS = Q / 4;
             bool ok = ptx::mbar_wait(&bar_ld[st], ((nch - 1 - c) >> 1) & 1, kWaitBudget);
             if (!ok) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
-            float phi = __ldg(prm.ck_phi + (ckb + c) * K + lane);
             const __nv_bfloat16* th = reinterpret_cast<const __nv_bfloat16*>(sbase + ST_TH);
-            for (int t = 0; t < Q; ++t) {
-                phi = red2pi(phi + __bfloat162float(th[t * K + lane]));
-                float s, co;
-                __sincosf(phi, &s, &co);
-                F[F_COS + t * K + lane] = co;
-                F[F_SIN + t * K + lane] = s;
+            float loc[QS];
+            float run = 0.0f;
+#pragma unroll
+            for (int q = 0; q < QS; ++q) {
+                run += __bfloat162float(th[(seg * QS + q) * K + lane]);
+                loc[q] = run;
+            }
+            F[F_SEG + seg * 32 + lane] = run;
+            ptx::bar_sync(1, 128);
+            float off = phi0;
+            for (int s2 = 0; s2 < seg; ++s2) off += F[F_SEG + s2 * 32 + lane];
+            off = red2pi(off);
+#pragma unroll
+            for (int q = 0; q < QS; ++q) {
+                float sn, co;
+                __sincosf(red2pi(off + loc[q]), &sn, &co);
+                F[F_COS + (seg * QS + q) * K + lane] = co;
+                F[F_SIN + (seg * QS + q) * K + lane] = sn;
             }
         }
         // ---- (2) the tiles are in; rotate B, C in place (B~, C~) and write B~' and C~'
@@ -373,23 +457,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        // ---- (3) batch 1
-        if (tid == 0) {
-            const uint32_t x_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_X), 16);
+        // ---- (3) S = C~ B~^T (commit: epilogue 1 waits for it and the products before
+        //      it); then dGu = C~'^T dY and dX := B~' dG, which need no mask
+        if (tid == 32) {
             const uint32_t b_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_B), 16);
             const uint32_t c_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_C), 16);
-            const uint32_t y_lo = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_DY), 16);
-            const uint32_t g_lo = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_G), 16);
-            const uint32_t d_lo = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DG), 16);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {   // K-major operands: 16 columns = +32 bytes
+            for (int k = 0; k < 4; ++k)
                 ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_S, c_lo + 2 * k, b_lo + 2 * k, kIdKK, k > 0);
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DSP, y_lo + 2 * k, x_lo + 2 * k, kIdKK, k > 0);
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_T2, y_lo + 2 * k, g_lo + 2 * k, kIdKK, k > 0);
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_XG, x_lo + 2 * k, d_lo + 2 * k, kIdKK, k > 0);
-            }
             ptx::umma_commit(&bar_m1);
+            const uint32_t y_mn = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_DY), TILE);
+            const uint32_t bd_k = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_BD), 16);
+            const uint32_t dg_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DG), TILE);
+            const uint32_t cd_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_CD), TILE);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {   // MN-major operands: 16 K rows = +2048 bytes
+                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DGU, cd_mn + 128 * k, y_mn + 128 * k, kIdMM, k > 0);
+                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DX, bd_k + 2 * k, dg_mn + 128 * k, kIdKM, k > 0);
+            }
         }
+        __syncwarp();
         if (!ptx::mbar_wait(&bar_m1, (nch - 1 - c) & 1, kWaitBudget)) {
             m3::set_status(m3::kStatusWaitTimeout);
             abort_s = 1;
@@ -469,45 +556,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         ptx::tc_fence_after();
         if (abort_s) { fail = true; break; }
-        // ---- (5) batch 2 (thread 0); meanwhile the token scalars (warp 4)
-        if (tid == 0) {
+        // ---- (5) the masked products (thread 32): dX += S'^T dY, dC~ = dS B~,
+        //      dB~ = dS^T C~; meanwhile the token scalars (warp 4) and the previous
+        //      chunk's dtheta (warps 6, 7)
+        if (tid == 32) {
             const uint32_t y_mn = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_DY), TILE);
             const uint32_t b_mn = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_B), TILE);
             const uint32_t c_mn = ptx::sdesc_lo(ptx::smem_u32(sbase + ST_C), TILE);
             const uint32_t sp_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_SP), TILE);
             const uint32_t ds_k = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DS), 16);
             const uint32_t ds_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DS), TILE);
-            const uint32_t bd_k = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_BD), 16);
-            const uint32_t dg_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_DG), TILE);
-            const uint32_t cd_mn = ptx::sdesc_lo(ptx::smem_u32(smem + OFF_CD), TILE);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {   // MN-major operands: 16 K rows = +2048 bytes
-                // dX = S'^T dY + B~' dG
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DX, sp_mn + 128 * k, y_mn + 128 * k, kIdMM, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DX, bd_k + 2 * k, dg_mn + 128 * k, kIdKM, 1);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DX, sp_mn + 128 * k, y_mn + 128 * k, kIdMM, 1);
                 ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DC, ds_k + 2 * k, b_mn + 128 * k, kIdKM, k > 0);
                 ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DB, ds_mn + 128 * k, c_mn + 128 * k, kIdMM, k > 0);
-                ptx::umma_bf16_lo<kDescHi, kDescHi>(tmem + TM_DGU, cd_mn + 128 * k, y_mn + 128 * k, kIdMM, k > 0);
             }
             ptx::umma_commit(&bar_m2);
         }
-        if (warp == 4) {
-            // column sums of dM o M and dM o E (lane: columns lane, lane + 32)
-            for (int u = 0; u < 2; ++u) {
-                float czm = 0.0f, cze = 0.0f;
-                for (int i = 0; i < 64; ++i) {
-                    czm += zm[i * 65 + lane + 32 * u];
-                    cze += ze[i * 65 + lane + 32 * u];
-                }
-                F[F_CZM + lane + 32 * u] = czm;
-                F[F_CZE + lane + 32 * u] = cze;
+        __syncwarp();
+        if (wg == 1) {
+            // column sums of dM o M (threads 128-191) and dM o E (192-255)
+            const int j = (tid - 128) & 63;
+            const float* src = (tid < 192) ? zm : ze;
+            float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < 64; i += 2) {
+                a0 += src[i * 65 + j];
+                a1 += src[(i + 1) * 65 + j];
             }
-            __syncwarp();
+            F[(tid < 192 ? F_CZM : F_CZE) + j] = a0 + a1;
+            ptx::bar_sync(2, 128);
+            if (warp >= 6 && prm.theta && c + 1 < nch) dtheta_chunk(c + 1);
+        }
+        if (warp == 4) {
             const float cs_end = F[F_CS + Q - 1];
             const float gdot = F[F_RED] + F[F_RED + 1] + F[F_RED + 2] + F[F_RED + 3];
             // per token (lane: tokens lane, lane + 32): dcs, dw, dgamma
@@ -626,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dA_acc += dA_c;
             }
         }
+        if (wg == 1) ptx::bar_sync(2, 128);   // dtheta has read F_DPR before epilogue 2 rewrites it
         if (!ptx::mbar_wait(&bar_m2, (nch - 1 - c) & 1, kWaitBudget)) {
             m3::set_status(m3::kStatusWaitTimeout);
             abort_s = 1;
@@ -698,27 +781,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        // ---- (7) dtheta: suffix sums over the chunk's tokens, carried from later chunks
-        if (warp == 6 && prm.theta) {
-            float acc = F[F_DPHI + lane];
-            for (int t = Q - 1; t >= 0; --t) {
-                float v = 0.0f;
-#pragma unroll
-                for (int r = 0; r < R; ++r) v += F[F_DPR + (t * R + r) * K + lane];
-                acc += v;
-                if (t < nt) prm.dtheta[tok_idx(t0 + t) * K + lane] = __float2bfloat16_rn(acc);
-            }
-            F[F_DPHI + lane] = acc;
-        }
         __syncthreads();
     }
+    // dtheta of chunk 0 (the last chunk processed)
+    if (!fail && warp >= 6 && prm.theta) dtheta_chunk(0);
     if (tid == 128) prm.dA_part[unit] = dA_acc;   // warp 4 lane 0 accumulated it
     if (fail && tid == 32) {
         // stopped early: wait (bounded) for the last load of each stage
         for (int s2 = 0; s2 < 2; ++s2)
             if (ld_count[s2] > 0) (void)ptx::mbar_wait(&bar_ld[s2], (ld_count[s2] - 1) & 1, kWaitBudget);
     }
-    if (fail && tid == 0) {
+    if (fail && tid == 32) {
         // every MMA issued has completed once this commit arrives
         ptx::umma_commit(&bar_fin);
         (void)ptx::mbar_wait(&bar_fin, 0, kWaitBudget);

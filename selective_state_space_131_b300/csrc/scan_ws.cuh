@@ -437,6 +437,9 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             //     are in, and Y_inter(c-1) = C~_{c-1} G_{c-2} -> TMEM Y_inter, which
             //     warpgroup 1 needs halfway through chunk c-1
             if (tid == kEarlyIssuer) issue_early(c);
+            // the issuing lane's warp reconverges before its other lanes wait: a lane
+            // parked in mbarrier.try_wait can hold back a diverged lane of its warp
+            __syncwarp();
 
             // (1) warp 0: chunk scalars for tokens lane (u = 0) and 32 + lane (u = 1):
             //     cs (log2 units), gamma, w, B~' row scale, mask column weights
@@ -738,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     ptx::umma_commit(&bar_sd[s]);
                 }
             }
+            __syncwarp();   // as above, for the S / dG issuer's warp
         }
         if (tid == kEarlyIssuer && !aborted && (nch >= 2 || prm.h0 != nullptr || prm.prev_B != nullptr))
             issue_early(nch);   // Y_inter(nch - 1)
@@ -889,6 +893,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                                                          id_y, k16 > 0);
                 ptx::umma_commit(&bar_y);
             }
+            __syncwarp();   // as above, for the Y_intra issuer's warp
             // (4) G_{c-1} is no longer read: store the bf16 copy of G_c
             fail = false;
             // chunk c has an inter-chunk term (always for a continuation); the flag is
