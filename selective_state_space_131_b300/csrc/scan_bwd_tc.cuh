@@ -54,10 +54,13 @@ constexpr int OFF_ZE = OFF_ZM + 64 * 65 * 4;   // fp32 [64][65]: dM o E (E = exp
 constexpr int OFF_F = OFF_ZE + 64 * 65 * 4;    // fp32 scratch, see below
 // float offsets inside OFF_F
 constexpr int F_CS = 0, F_GAM = 64, F_W = 128, F_S = 192, F_ECS = 256, F_EEND = 320;     // per token
-constexpr int F_COS = 384, F_SIN = F_COS + 64 * 32;                                      // [Q][32]
-constexpr int F_RZM = F_SIN + 64 * 32, F_RG = F_RZM + 64, F_EBAR = F_RG + 64, F_DSR = F_EBAR + 64;   // per row
-constexpr int F_DPR = F_DSR + 64;                                                        // [64 rows][32 pairs]
-constexpr int F_DL = F_DPR + 64 * 32;                                                    // [2][dt | lam][68]
+// [row or token][pair] arrays use a row stride of KS = 33 floats: threads that walk
+// rows at a fixed pair then hit distinct banks
+constexpr int KS = 33;
+constexpr int F_COS = 384, F_SIN = F_COS + 64 * KS;                                      // [Q][KS]
+constexpr int F_RZM = F_SIN + 64 * KS, F_RG = F_RZM + 64, F_EBAR = F_RG + 64, F_DSR = F_EBAR + 64;   // per row
+constexpr int F_DPR = F_DSR + 64;                                                        // [64 rows][KS]
+constexpr int F_DL = F_DPR + 64 * KS;                                                    // [2][dt | lam][68]
 constexpr int F_RED = F_DL + 2 * 2 * 68;                                                 // [8]: <dG, G> partials
 constexpr int F_PEND = F_RED + 8;                                                        // ddt, dlam, dA
 constexpr int F_DPHI = F_PEND + 4;                                                       // [32] dtheta suffix carry
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = seg * QS + q;
             float a = 0.0f;
 #pragma unroll
-            for (int r = 0; r < R; ++r) a += F[F_DPR + (t * R + r) * K + lane];
+            for (int r = 0; r < R; ++r) a += F[F_DPR + (t * R + r) * KS + lane];
             v[q] = a;
             tot += a;
         }
@@ -404,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < QS; ++q) {
                 float sn, co;
                 __sincosf(red2pi(off + loc[q]), &sn, &co);
-                F[F_COS + (seg * QS + q) * K + lane] = co;
-                F[F_SIN + (seg * QS + q) * K + lane] = sn;
+                F[F_COS + (seg * QS + q) * KS + lane] = co;
+                F[F_SIN + (seg * QS + q) * KS + lane] = sn;
             }
         }
         // ---- (2) the tiles are in; rotate B, C in place (B~, C~) and write B~' and C~'
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float b0 = lo16(pb[m]), b1 = hi16(pb[m]), c0 = lo16(pc[m]), c1 = hi16(pc[m]);
                     if (prm.theta) {
                         const int k = g * 4 + m;
-                        const float co = F[F_COS + t * K + k], si = F[F_SIN + t * K + k];
+                        const float co = F[F_COS + t * KS + k], si = F[F_SIN + t * KS + k];
                         // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
                         const float nb0 = fmaf(b0, co, b1 * si), nb1 = fmaf(-b0, si, b1 * co);
                         const float nc0 = fmaf(c0, co, c1 * si), nc1 = fmaf(-c0, si, c1 * co);
@@ -755,14 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float dc0 = __uint_as_float(vc[2 * m]) + eT[2 * m], dc1 = __uint_as_float(vc[2 * m + 1]) + eT[2 * m + 1];
                 const float db0 = __uint_as_float(vb[2 * m]) + sX[2 * m], db1 = __uint_as_float(vb[2 * m + 1]) + sX[2 * m + 1];
                 float co = 1.0f, si = 0.0f;
-                if (prm.theta) { co = F[F_COS + t * K + k]; si = F[F_SIN + t * K + k]; }
+                if (prm.theta) { co = F[F_COS + t * KS + k]; si = F[F_SIN + t * KS + k]; }
                 // dB = Rot(+phi) dB~: (a cos - b sin, a sin + b cos)
                 oc[2 * m] = fmaf(dc0, co, -dc1 * si);
                 oc[2 * m + 1] = fmaf(dc0, si, dc1 * co);
                 ob[2 * m] = fmaf(db0, co, -db1 * si);
                 ob[2 * m + 1] = fmaf(db0, si, db1 * co);
                 // d/dphi Rot(-phi) v = (v~_1, -v~_0)
-                F[F_DPR + row * K + k] = db0 * br[2 * m + 1] - db1 * br[2 * m] + dc0 * cr[2 * m + 1] - dc1 * cr[2 * m];
+                F[F_DPR + row * KS + k] = db0 * br[2 * m + 1] - db1 * br[2 * m] + dc0 * cr[2 * m + 1] - dc1 * cr[2 * m];
             }
             if (t < nt) {
                 const int64_t gi = (tok_idx(t0 + t) * R + (row - t * R)) * 64 + 32 * hc;
