@@ -41,9 +41,13 @@ HBM_FALLBACK_GBS = 6400.0
 # source is unchanged, else null.  Captured at T = 2048 and scaled x4 to
 # T = 8192 (traffic grows with the sequence length).
 NCU_TRAFFIC = {
-    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.210240e6 + 48.293120e6),
+    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.188224e6 + 49.031424e6),
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
-                                      "sha256": "bc29f03bb103d091"},
+                                      "sha256": "dc6d5e6015abf56b"},
+    # decode: one step of the 1024-step sweep (graph replay), per launch
+    "decode_f32_b256h32P64N64_R1": {"bytes": 145.835264e6 + 77.099520e6,
+                                    "source": "selective_state_space_131_b300/csrc/step_fast.cuh",
+                                    "sha256": "dcdb0919045c3efd"},
 }
 
 
@@ -628,6 +632,10 @@ def main():
         for r in (1, 4):
             dr = bench_decode(m3, stream, args.decode_steps, rank, rank=r)
             dr["roofline_frac"] = dr["GB_per_s"] / peaks["hbm_gbs"]
+            dr["traffic"] = ncu_traffic(dr["workload"])
+            if dr["traffic"]:
+                dr["dram_GB_per_s"] = dr["traffic"] / (dr["us_per_step"] * 1e-6) / 1e9
+                dr["dram_frac"] = dr["dram_GB_per_s"] / peaks["hbm_gbs"]
             dec[f"R{r}"] = dr
         for r in (1, 4):
             dk = bench_decode_k(m3, stream, args.decode_steps, rank, rank=r, k=args.decode_k)
