@@ -214,23 +214,31 @@ inline size_t smem_bytes(int64_t N, int64_t P, int64_t R) { return (size_t)(thre
 // ---------------------------------------------------------------------------
 // Multi-token decode (m3_step_k): k consecutive tokens of every (b, h) in one
 // launch, the state read once and written once.  The thread tiling of
-// m3_step_fast_kernel; the state stays in registers across the k tokens.  The
-// tokens' inputs are staged in shared memory in groups of kGroup with 16-byte
-// cp.async copies, so the global latency is paid once per group rather than
-// per token: group 0 (and the caller's previous token) before the state loads,
-// group g + 1 as soon as the first token of group g is done (two buffers; the
-// previous token of group g's first token is the last of group g - 1).  Each
-// token's y meets in a double-buffered shared-memory reduction (one barrier per
-// token).  Token tensors have the prefill's token-major layout: x [b, k, h, R, P],
+// m3_step_fast_kernel; the state stays in registers across the k tokens.
+//
+// The recurrence is carried in the augmented form
+//   g_{j-1} = h'_{j-1} + c_j u_{j-1},   c_j = (1 - lambda_j) dt_j  (so beta_j = c_j alpha_j)
+//   h'_j    = alpha_j Rot(theta_j) g_{j-1} + gamma_j u_j,   y_j = C_j^T h'_j
+//   g_j     = h'_j + c_{j+1} u_j
+// which needs no previous-token product per token (the caller's previous token
+// enters once, in g_{-1}); the state written back is h' of the last token.
+// The tokens' inputs are staged in shared memory in groups of kGroup with
+// 16-byte cp.async copies (the latency is paid once per group, the next group
+// loads while this one runs); at the start of a group the threads turn its
+// angles and decays into alpha cos / alpha sin per (token, pair) and gamma, c
+// per token, once for the whole CTA.  Each token's y meets in a
+// double-buffered shared-memory reduction (one barrier per token).  Token
+// tensors have the prefill's token-major layout: x [b, k, h, R, P],
 // B / C [b, k, h, R, N], theta [b, k, h, N/2], dt / lambda [b, k, h].
 constexpr int kGroup = 8;
 
 struct StepKArgs {
     int H, N, P, P4;
     int64_t k;
-    // staging layout (bytes): per token x | B | C | theta | dt, lambda; the
-    // previous-token slot x | B; nbuf group buffers of kGroup tokens
-    int xb, nb, kb, tokb, nbuf;
+    // staging layout (bytes): per token x | B | C | theta | dt, lambda; per group
+    // buffer also dt, lambda of the token after the group; the previous-token
+    // slot x | B; nbuf group buffers; the coefficients of one group
+    int xb, nb, kb, tokb, grpb, nbuf;
 };
 
 inline StepKArgs stepk_layout(int H, int N, int P, int R, int64_t k, int es) {
@@ -241,14 +249,17 @@ inline StepKArgs stepk_layout(int H, int N, int P, int R, int64_t k, int es) {
     a.nb = up16(R * N * es);
     a.kb = up16((N / 2) * es);
     a.tokb = a.xb + 2 * a.nb + a.kb + 16;
+    a.grpb = kGroup * a.tokb + 16;
     a.nbuf = k > kGroup ? 2 : 1;
     return a;
 }
 // Dynamic shared memory of m3_step_k_kernel: the y reduction (2 x warps x R x P
-// floats), the previous-token slot and the group buffers.
+// floats), the previous-token slot, the group buffers and one group's
+// coefficients (alpha cos, alpha sin per token and pair; gamma, c per token).
 inline size_t stepk_smem(const StepKArgs& a, int R) {
     const int warps = (a.P4 * (a.N / kRPT)) / 32;
-    return (size_t)2 * warps * R * a.P * 4 + (size_t)(a.xb + a.nb) + (size_t)a.nbuf * kGroup * a.tokb;
+    return (size_t)2 * warps * R * a.P * 4 + (size_t)(a.xb + a.nb) + (size_t)a.nbuf * a.grpb +
+           (size_t)kGroup * (a.N / 2) * 8 + (size_t)kGroup * 8;
 }
 
 template <typename T>
@@ -260,6 +271,7 @@ struct SVec<float> {
         o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
     }
     static __device__ __forceinline__ float2 ld2(const uint8_t* p) { return *reinterpret_cast<const float2*>(p); }
+    static __device__ __forceinline__ float ld1(const uint8_t* p) { return *reinterpret_cast<const float*>(p); }
 };
 template <>
 struct SVec<__nv_bfloat16> {
@@ -272,6 +284,9 @@ struct SVec<__nv_bfloat16> {
         const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
         return make_float2(Vec<__nv_bfloat16>::lo(u), Vec<__nv_bfloat16>::hi(u));
     }
+    static __device__ __forceinline__ float ld1(const uint8_t* p) {
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+    }
 };
 
 template <typename T, int R, int MAXT>
@@ -282,7 +297,7 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                                                         const T* __restrict__ theta, const T* __restrict__ prev_B,
                                                         const T* __restrict__ prev_x, T* __restrict__ y) {
     extern __shared__ __align__(16) float red[];   // [2][warps][R][P], then the staging area
-    const int N = a.N, P = a.P, P4 = a.P4, H = a.H;
+    const int N = a.N, P = a.P, P4 = a.P4, H = a.H, K = N / 2;
     constexpr int es = sizeof(T);
     if ((int)blockDim.x != P4 * (N / kRPT)) {
         if (threadIdx.x == 0) m3::set_status(m3::kStatusBadLaunch);
@@ -299,14 +314,16 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
     float* st = state + unit * (int64_t)N * P + (int64_t)n0 * P + p0;
     uint8_t* prev_slot = reinterpret_cast<uint8_t*>(red + 2 * nwarps * R * P);
     uint8_t* bufs = prev_slot + a.xb + a.nb;
+    float* coef = reinterpret_cast<float*>(bufs + (size_t)a.nbuf * a.grpb);   // [kGroup][K][2]
+    float* tokc = coef + kGroup * K * 2;                                       // [kGroup][gamma, c_next]
     const int64_t ngroups = (a.k + kGroup - 1) / kGroup;
     const bool has_theta = theta != nullptr;
     const bool theta16 = ((N / 2) * es) % 16 == 0;
 
-    // token j's slot in the staging area
-    auto slot = [&](int64_t j) { return bufs + (size_t)((j / kGroup) % a.nbuf) * kGroup * a.tokb + (j % kGroup) * a.tokb; };
-    // issue the copies of group gi's tokens (every thread takes a share; lambda = NULL
-    // is written as 1 directly)
+    auto gbuf = [&](int64_t gi) { return bufs + (size_t)(gi % a.nbuf) * a.grpb; };
+    auto slot = [&](int64_t j) { return gbuf(j / kGroup) + (j % kGroup) * a.tokb; };
+    // issue the copies of group gi's tokens, and dt / lambda of the token after it
+    // (every thread takes a share; lambda = NULL is written as 1 directly)
     auto issue_group = [&](int64_t gi) {
         const int64_t j0 = gi * kGroup;
         const int nt = (int)((a.k - j0) < kGroup ? (a.k - j0) : kGroup);
@@ -338,11 +355,24 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
             else if (lam) ptx::cp_async4(ds + 1, lam + tj, true);
             else ds[1] = 1.0f;
         }
+        if (threadIdx.x == 0) {
+            float* nx = reinterpret_cast<float*>(gbuf(gi) + kGroup * a.tokb);
+            const int64_t jn = j0 + kGroup;
+            if (jn < a.k) {
+                const int64_t tn = (b * a.k + jn) * H + h;
+                ptx::cp_async4(nx, dt + tn, true);
+                if (lam) ptx::cp_async4(nx + 1, lam + tn, true);
+                else nx[1] = 1.0f;
+            } else {
+                nx[0] = 0.0f;
+                nx[1] = 1.0f;
+            }
+        }
     };
 
     // the caller's previous token and group 0, then the state (the bulk of the bytes)
-    const bool has_prev0 = prev_B != nullptr;
-    if (has_prev0) {
+    const bool has_prev = prev_B != nullptr;
+    if (has_prev) {
         for (int c = threadIdx.x; c < a.xb / 16 + (R * N * es) / 16; c += nthr) {
             if (c < a.xb / 16) ptx::cp_async16(prev_slot + c * 16, reinterpret_cast<const uint8_t*>(prev_x + unit * R * P) + c * 16);
             else ptx::cp_async16(prev_slot + a.xb + (c - a.xb / 16) * 16,
@@ -356,99 +386,129 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
     for (int i = 0; i < kRPT; ++i) hs[i] = __ldcs(reinterpret_cast<const float4*>(st + (int64_t)i * P));
     const float A_h = __ldg(A + h);
 
-    for (int64_t j = 0; j < a.k; ++j) {
-        if (j % kGroup == 0) {
-            ptx::cp_async_wait_all();   // this group's copies (the only ones in flight)
-            __syncthreads();
-        }
-        const uint8_t* cur = slot(j);
-        const bool has_prev = (j > 0) || has_prev0;
-        const uint8_t* prv = j > 0 ? slot(j - 1) : prev_slot;
-        const float* sc = reinterpret_cast<const float*>(cur + a.xb + 2 * a.nb + a.kb);
-        const float d = sc[0], l = sc[1];
-        const float alpha = expf(d * A_h);
-        const float beta = (1.0f - l) * d * alpha;
-        const float gamma = l * d;
-        float xr[R][4], pxr[R][4];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            SVec<T>::ld4(cur + (r * P + p0) * es, xr[r]);
-            if (has_prev) {
-                SVec<T>::ld4(prv + (r * P + p0) * es, pxr[r]);
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) pxr[r][jj] = 0.0f;
-            }
-        }
-        float cs[kRPT / 2], sn[kRPT / 2];
-        {
-            float th[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (has_theta) SVec<T>::ld4(cur + a.xb + 2 * a.nb + (n0 / 2) * es, th);
-#pragma unroll
-            for (int m = 0; m < kRPT / 2; ++m) __sincosf(reduce_2pi(th[m]), &sn[m], &cs[m]);
-        }
-        float yp[R][4];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) yp[r][jj] = 0.0f;
-#pragma unroll
-        for (int m = 0; m < kRPT / 2; ++m) {
-            float* h0 = reinterpret_cast<float*>(&hs[2 * m]);
-            float* h1 = reinterpret_cast<float*>(&hs[2 * m + 1]);
-            float2 br[R], pbr[R], cr[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                br[r] = SVec<T>::ld2(cur + a.xb + (r * N + n0 + 2 * m) * es);
-                cr[r] = SVec<T>::ld2(cur + a.xb + a.nb + (r * N + n0 + 2 * m) * es);
-                pbr[r] = has_prev ? SVec<T>::ld2(prv + a.xb + (r * N + n0 + 2 * m) * es) : make_float2(0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                float v0 = 0.0f, v1 = 0.0f, u0 = 0.0f, u1 = 0.0f;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    v0 = fmaf(pbr[r].x, pxr[r][jj], v0);
-                    v1 = fmaf(pbr[r].y, pxr[r][jj], v1);
-                    u0 = fmaf(br[r].x, xr[r][jj], u0);
-                    u1 = fmaf(br[r].y, xr[r][jj], u1);
-                }
-                const float z0 = fmaf(alpha, h0[jj], beta * v0);
-                const float z1 = fmaf(alpha, h1[jj], beta * v1);
-                const float o0 = fmaf(gamma, u0, fmaf(cs[m], z0, -sn[m] * z1));
-                const float o1 = fmaf(gamma, u1, fmaf(sn[m], z0, cs[m] * z1));
-                h0[jj] = o0;
-                h1[jj] = o1;
-#pragma unroll
-                for (int r = 0; r < R; ++r) yp[r][jj] = fmaf(cr[r].x, o0, fmaf(cr[r].y, o1, yp[r][jj]));
-            }
-        }
-        // y of token j: lanes P4 apart, then the warps through shared memory
-#pragma unroll
-        for (int o = P4; o < 32; o <<= 1)
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) yp[r][jj] += __shfl_xor_sync(0xffffffffu, yp[r][jj], o);
-        float* rb = red + (j & 1) * nwarps * R * P;
-        if (lane < P4) {
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                *reinterpret_cast<float4*>(rb + (warp * R + r) * P + p0) =
-                    make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
-        }
+    for (int64_t gi = 0; gi < ngroups; ++gi) {
+        const int64_t j0 = gi * kGroup;
+        const int nt = (int)((a.k - j0) < kGroup ? (a.k - j0) : kGroup);
+        ptx::cp_async_wait_all();   // group gi (the only copies in flight)
         __syncthreads();
-        // the first token of a group is done: every read of the group before it has
-        // happened, so the next group can land in that buffer
-        if (j % kGroup == 0 && j / kGroup + 1 < ngroups) {
-            issue_group(j / kGroup + 1);
+        // the group's coefficients: alpha cos, alpha sin per (token, pair); gamma and
+        // c of the next token per token
+        for (int e = threadIdx.x; e < nt * K; e += nthr) {
+            const int jj = e / K, k = e - jj * K;
+            const uint8_t* d = slot(j0 + jj);
+            const float* sc = reinterpret_cast<const float*>(d + a.xb + 2 * a.nb + a.kb);
+            const float al = expf(sc[0] * A_h);
+            float sn = 0.0f, cs = 1.0f;
+            if (has_theta) __sincosf(reduce_2pi(SVec<T>::ld1(d + a.xb + 2 * a.nb + k * es)), &sn, &cs);
+            *reinterpret_cast<float2*>(coef + (jj * K + k) * 2) = make_float2(al * cs, al * sn);
+        }
+        for (int jj = threadIdx.x; jj < nt; jj += nthr) {
+            const float* sc = reinterpret_cast<const float*>(slot(j0 + jj) + a.xb + 2 * a.nb + a.kb);
+            const float* sn = (jj + 1 < kGroup) ? reinterpret_cast<const float*>(slot(j0 + jj + 1) + a.xb + 2 * a.nb + a.kb)
+                                                : reinterpret_cast<const float*>(gbuf(gi) + kGroup * a.tokb);
+            // the token after the last of the call does not exist: c = 0
+            const bool last = j0 + jj + 1 >= a.k;
+            tokc[2 * jj] = sc[1] * sc[0];
+            tokc[2 * jj + 1] = last ? 0.0f : (1.0f - sn[1]) * sn[0];
+        }
+        if (gi == 0 && has_prev) {
+            // g_{-1} = h'_{-1} + c_0 u_{-1}: the caller's previous token enters here once
+            const float* s0 = reinterpret_cast<const float*>(slot(0) + a.xb + 2 * a.nb + a.kb);
+            const float c0 = (1.0f - s0[1]) * s0[0];
+            float px[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) SVec<T>::ld4(prev_slot + (r * P + p0) * es, px[r]);
+#pragma unroll
+            for (int i = 0; i < kRPT; ++i) {
+                float* hv = reinterpret_cast<float*>(&hs[i]);
+                float bb[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) bb[r] = SVec<T>::ld1(prev_slot + a.xb + (r * N + n0 + i) * es);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float u = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) u = fmaf(bb[r], px[r][jj], u);
+                    hv[jj] = fmaf(c0, u, hv[jj]);
+                }
+            }
+        }
+        // the next group loads while this one runs (its buffer held group gi - 1)
+        if (gi + 1 < ngroups) {
+            issue_group(gi + 1);
             ptx::cp_async_commit();
         }
-        const int64_t tj = (b * a.k + j) * H + h;
-        for (int e = threadIdx.x; e < R * P; e += nthr) {
-            float acc = 0.0f;
-            for (int w = 0; w < nwarps; ++w) acc += rb[w * R * P + e];
-            Vec<T>::st(y + tj * R * P + e, acc);
+        __syncthreads();
+
+        for (int jj = 0; jj < nt; ++jj) {
+            const int64_t j = j0 + jj;
+            const uint8_t* cur = slot(j);
+            const float2 gc = *reinterpret_cast<const float2*>(tokc + 2 * jj);   // gamma, c_next
+            float cf[8];
+            {
+                const float4 c0 = *reinterpret_cast<const float4*>(coef + (jj * K + n0 / 2) * 2);
+                const float4 c1 = *reinterpret_cast<const float4*>(coef + (jj * K + n0 / 2) * 2 + 4);
+                cf[0] = c0.x; cf[1] = c0.y; cf[2] = c0.z; cf[3] = c0.w;
+                cf[4] = c1.x; cf[5] = c1.y; cf[6] = c1.z; cf[7] = c1.w;
+            }
+            const bool upd = j + 1 < a.k;   // the last token leaves h', not g
+            float xr[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) SVec<T>::ld4(cur + (r * P + p0) * es, xr[r]);
+            float yp[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int jx = 0; jx < 4; ++jx) yp[r][jx] = 0.0f;
+#pragma unroll
+            for (int m = 0; m < kRPT / 2; ++m) {
+                float* h0 = reinterpret_cast<float*>(&hs[2 * m]);
+                float* h1 = reinterpret_cast<float*>(&hs[2 * m + 1]);
+                float2 br[R], cr[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    br[r] = SVec<T>::ld2(cur + a.xb + (r * N + n0 + 2 * m) * es);
+                    cr[r] = SVec<T>::ld2(cur + a.xb + a.nb + (r * N + n0 + 2 * m) * es);
+                }
+                const float ac = cf[2 * m], as = cf[2 * m + 1];
+#pragma unroll
+                for (int jx = 0; jx < 4; ++jx) {
+                    float u0 = 0.0f, u1 = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        u0 = fmaf(br[r].x, xr[r][jx], u0);
+                        u1 = fmaf(br[r].y, xr[r][jx], u1);
+                    }
+                    // alpha Rot(theta) g + gamma u: (a, b) -> (ac a - as b, as a + ac b)
+                    const float o0 = fmaf(gc.x, u0, fmaf(ac, h0[jx], -as * h1[jx]));
+                    const float o1 = fmaf(gc.x, u1, fmaf(as, h0[jx], ac * h1[jx]));
+#pragma unroll
+                    for (int r = 0; r < R; ++r) yp[r][jx] = fmaf(cr[r].x, o0, fmaf(cr[r].y, o1, yp[r][jx]));
+                    h0[jx] = upd ? fmaf(gc.y, u0, o0) : o0;
+                    h1[jx] = upd ? fmaf(gc.y, u1, o1) : o1;
+                }
+            }
+            // y of token j: lanes P4 apart, then the warps through shared memory
+#pragma unroll
+            for (int o = P4; o < 32; o <<= 1)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int jx = 0; jx < 4; ++jx) yp[r][jx] += __shfl_xor_sync(0xffffffffu, yp[r][jx], o);
+            float* rb = red + (j & 1) * nwarps * R * P;
+            if (lane < P4) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    *reinterpret_cast<float4*>(rb + (warp * R + r) * P + p0) =
+                        make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
+            }
+            __syncthreads();
+            const int64_t tj = (b * a.k + j) * H + h;
+            for (int e = threadIdx.x; e < R * P; e += nthr) {
+                float acc = 0.0f;
+                for (int w = 0; w < nwarps; ++w) acc += rb[w * R * P + e];
+                Vec<T>::st(y + tj * R * P + e, acc);
+            }
         }
     }
 #pragma unroll
