@@ -156,3 +156,25 @@ def test_bwd_empty_sequence(m3):
                    None, None, None, None, None, 0, dims=dims)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dA).item() == 0
+
+
+EDGE_KINDS = ["fast_decay", "a_zero", "lambda_zero", "lambda_one", "tiny_dt", "mixed", "large_phi"]
+
+
+@pytest.mark.parametrize("kind", EDGE_KINDS)
+@pytest.mark.parametrize("dtype,P,N,R,chunk", [("bf16", 64, 64, 1, 64), ("bf16", 64, 64, 4, 16),
+                                               ("f32", 16, 16, 2, 32)], ids=lambda v: str(v))
+def test_bwd_edges(m3, kind, dtype, P, N, R, chunk):
+    """The forced edge cases of test_gpu_edges through the backward pass: the
+    tensor-core path (bf16 N = P = 64) and the CUDA-core path (fp32)."""
+    from tests.test_gpu_edges import apply_edge
+    shape = inputs.ScanShape(batch=2, seqlen=150, heads=3, headdim=P, dstate=N, rank=R, chunk=chunk, dtype=dtype)
+    inp = apply_edge(inputs.make_scan_inputs(shape, 950 + R), kind, 951 + R, dtype, R)
+    dy, dfinal = upstream(shape, 952)
+    got = gpu_bwd(m3, inp, dy, dfinal, chunk)
+    ref = oracle.scan_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["lam"], inp["theta"], dy, dfinal)
+    for k in GRADS:
+        if got[k] is not None:
+            assert torch.isfinite(got[k]).all(), k
+    errs = compare(got, ref, TOL[dtype], kind)
+    print(kind, dtype, R, {k: f"{v:.1e}" for k, v in errs.items()})

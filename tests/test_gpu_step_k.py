@@ -170,3 +170,15 @@ def test_step_k_decode_workload_1024_tokens(m3, R):
         ey = max_rel(yg[t0 - 1:t1 - 1].transpose(0, 1), yr)
         es = max_rel(snaps[s][bsel][:, hsel].cpu(), h)
         assert ey <= 1e-4 and es <= 1e-4, (s, ey, es)
+
+
+@pytest.mark.parametrize("kind", ["fast_decay", "a_zero", "lambda_zero", "lambda_one", "tiny_dt", "large_phi"])
+@pytest.mark.parametrize("R", [1, 4])
+def test_step_k_edges(m3, kind, R):
+    """The forced edge cases of test_gpu_edges over a 12-token launch (fp32)."""
+    from tests.test_gpu_edges import apply_edge
+    toks, s0, pB, pX = make_case(3, 4, 64, 64, R, 12, "f32", 770 + R)
+    toks = apply_edge(toks, kind, 771 + R, "f32", R)
+    y, st = run_k(m3, toks, s0, pB, pX)
+    yr, fr = oracle_k(toks, s0, pB, pX)
+    assert max_rel(y, yr) <= 1e-4 and max_rel(st, fr) <= 1e-4, kind
