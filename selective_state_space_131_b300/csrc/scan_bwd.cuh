@@ -24,7 +24,10 @@
 //   the rotation: B~ = Rot(-Phi) B gives dB = Rot(Phi) dB~ and
 //   dPhi_t = sum_r (dB~_0 B~_1 - dB~_1 B~_0 + dC~_0 C~_1 - dC~_1 C~_0) per pair,
 //   dtheta_t = sum_{t' >= t} dPhi_t' (a suffix sum carried across chunks, started
-//   by the final state's rotation).
+//   by the final state's rotation).  Pairs whose relative angle is zero -- a token
+//   with itself, the last token with the final state -- enter neither dPhi nor the
+//   start of the sum: their two contributions cancel exactly, and summed they would
+//   leave rounding noise of their own size in gradients that fast decay makes tiny.
 //
 // Pass 1 (m3_bwd_ckpt_kernel) recomputes the chunk states forward and stores
 // G_{c-1} for every chunk and G_last, with the angle at each chunk start, in the
@@ -52,13 +55,13 @@ struct Geo {
     int H, nch;
     // pass 2
     int o_x, o_dy, o_bt, o_ct, o_s, o_ds, o_z, o_g, o_dg, o_t2, o_xg, o_cos, o_sin, o_tok, o_row, o_dl, o_red,
-        o_pend, o_dp, bytes;
+        o_pend, o_dp, o_sp, bytes;
     // pass 1
     int c_bt, c_x, c_g, c_cos, c_sin, c_tok, c_dl, c_bytes;
 };
 
 // Per-token scalar slots (floats) of pass 2, each [Q]
-enum { kCs = 0, kGam, kW, kS, kEcs, kDcs, kDw, kDg, kCsdt, kTokSlots };
+enum { kCs = 0, kGam, kW, kS, kEcs, kDcs, kDw, kDg, kCsdt, kXs, kTokSlots };
 // Per-row slots (floats), each [QR]
 enum { kEbar = 0, kDsr, kRowSlots };
 
@@ -89,6 +92,7 @@ inline Geo make_geo(int64_t T, int H, int P, int N, int R, int Q) {
     g.o_red = take(kThreads + 4);
     g.o_pend = take(4 + g.K);   // pending ddt / dlambda of the next chunk's first token, dA; dPhi suffix carry
     g.o_dp = take(g.QR * g.K);  // dPhi share of every row and pair
+    g.o_sp = take(g.QR * g.K);  // last chunk: the final state's pair with every row
     g.bytes = (o + 15) & ~15;
     o = 0;
     g.c_bt = take(g.QR * g.NS);
@@ -126,8 +130,10 @@ inline Work work_split(void* ws, int64_t units, const Geo& g) {
     return w;
 }
 
-// Warp 0: chunk-local cs (natural-log units) of the Q tokens from s_dt into cs[].
-__device__ __forceinline__ void chunk_cs(const float* s_dt, float A_h, int Q, float* cs, int lane) {
+// Warp 0: chunk-local cs (natural-log units) of the Q tokens from s_dt into cs[];
+// past the nt valid tokens cs repeats the last one's value bit for bit (the scan's
+// rounding would not), so that exp(cs_end - cs_t) is exactly 1 for the last token.
+__device__ __forceinline__ void chunk_cs(const float* s_dt, float A_h, int Q, int nt, float* cs, int lane) {
     const int m = (Q + 31) / 32;
     float run = 0.0f;
     for (int i = 0; i < m; ++i) {
@@ -147,6 +153,8 @@ __device__ __forceinline__ void chunk_cs(const float* s_dt, float A_h, int Q, fl
             cs[t] = acc;
         }
     }
+    __syncwarp();
+    for (int t = nt + lane; t < Q; t += 32) cs[t] = cs[nt - 1];
     __syncwarp();
 }
 
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_ckpt_kernel(const Geo geo, Wo
         }
         __syncthreads();
         if (tid < 32) {
-            chunk_cs(s_dt, A_h, Q, cs, tid);
+            chunk_cs(s_dt, A_h, Q, nt, cs, tid);
             const float cs_end = cs[Q - 1];
             for (int t = tid; t < Q; t += 32) {
                 const float w = s_lam[t] * s_dt[t] + (1.0f - s_lam[t + 1]) * s_dt[t + 1];
@@ -291,6 +299,7 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
     float* pend = reinterpret_cast<float*>(smem + geo.o_pend);   // [0] ddt, [1] dlam of token c0 + Q; [2] dA
     float* dphi_c = pend + 4;                                     // [K] suffix sum of dPhi
     float* dpr = reinterpret_cast<float*>(smem + geo.o_dp);       // [QR][K]
+    float* spr = reinterpret_cast<float*>(smem + geo.o_sp);       // [QR][K]
     float* cs = tok + kCs * Q;
     float* gam = tok + kGam * Q;
     float* wv = tok + kW * Q;
@@ -300,14 +309,20 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
     float* dw = tok + kDw * Q;
     float* dgm = tok + kDg * Q;
     float* csdt = tok + kCsdt * Q;
+    float* xs = tok + kXs * Q;
     float* ebar = rowv + kEbar * QR;
     float* dsr = rowv + kDsr * QR;
     auto tok_idx = [&](int64_t t) { return (b * Tn + t) * H + h; };
     const float* Gin = wk.G + unit * (int64_t)(nch + 1) * N * P;
     const float* Pin = wk.phi + unit * (int64_t)(nch + 1) * K;
 
-    // dG_last = Rot(-Phi_{T-1}) dfinal; the final rotation's angle gradient
-    // sum_p (-df_0 f_1 + df_1 f_0), f = Rot(Phi_{T-1}) G_last, starts the dtheta suffix sum
+    // dG_last = Rot(-Phi_{T-1}) dfinal.  The final rotation's angle gradient
+    // sum_p (-df_0 f_1 + df_1 f_0), f = Rot(Phi_{T-1}) G_last, starts the dtheta suffix
+    // sum; it is formed in parts: here the part through G_{nch-1} (f = Rot(Phi_{T-1})
+    // G_{nch-1}, decayed by the last chunk's exp(cs_end) once that is known), and in the
+    // last chunk the part through each of its rows (minus that row's s-term share of
+    // dPhi), without the last token's rows, whose pair with the final state has zero
+    // angle and cancels exactly
     for (int e = tid; e < K * P; e += kThreads) {
         const int k = e / P, p = e % P;
         float df0 = 0.0f, df1 = 0.0f;
@@ -319,8 +334,9 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
         if (theta) sincosf(Pin[(int64_t)nch * K + k], &sn, &cn);
         dG[(2 * k) * PS + p] = fmaf(df0, cn, df1 * sn);
         dG[(2 * k + 1) * PS + p] = fmaf(-df0, sn, df1 * cn);
-        // f = Rot(Phi) G_last, staged in G for the angle term below
-        const float g0 = Gin[(int64_t)nch * N * P + (2 * k) * P + p], g1 = Gin[(int64_t)nch * N * P + (2 * k + 1) * P + p];
+        // f = Rot(Phi) G_{nch-1}, staged in G for the angle term below
+        const float* gl = Gin + (int64_t)(nch - 1) * N * P;
+        const float g0 = gl[(2 * k) * P + p], g1 = gl[(2 * k + 1) * P + p];
         G[(2 * k) * PS + p] = -df0 * fmaf(g0, sn, g1 * cn) + df1 * fmaf(g0, cn, -g1 * sn);
     }
     if (tid == 0) { pend[0] = 0.0f; pend[1] = 0.0f; pend[2] = 0.0f; }
@@ -364,7 +380,7 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
         __syncthreads();
         // ---- (2) scalars (warp 0) and angles (one thread per pair)
         if (tid < 32) {
-            chunk_cs(s_dt, A_h, Q, cs, tid);
+            chunk_cs(s_dt, A_h, Q, nt, cs, tid);
             const float cs_end = cs[Q - 1];
             for (int t = tid; t < Q; t += 32) {
                 gam[t] = s_lam[t] * s_dt[t];
@@ -462,15 +478,54 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
             acc = fmaf(sv[tj], st, acc);
             if (tj < nt) m3::IO<T>::st(dx, tok_idx(t0 + tj) * R * P + (j - tj * R) * P + p, acc);
         }
-        for (int e = tid; e < QR * N; e += kThreads) {
-            const int i = e / N, n = e % N, ti = i / R;
-            float acc = 0.0f;
-            const int jn = (ti + 1) * R;
-            for (int j = 0; j < jn; ++j) acc = fmaf(dS[i * QS + j], Bt[j * NS + n], acc);
-            T2[i * NS + n] = fmaf(ecs[ti], T2[i * NS + n], acc);
-            float accb = 0.0f;
-            for (int i2 = ti * R; i2 < QR; ++i2) accb = fmaf(dS[i2 * QS + i], Ct[i2 * NS + n], accb);
-            XG[i * NS + n] = fmaf(sv[ti], XG[i * NS + n], accb);
+        // dC~_i = sum_j dS_ij B~_j + exp(cs_i) T2_i and dB~_j = sum_i dS_ij C~_i + s_j XG_j,
+        // one thread per row and rotation pair.  The same-token block's share (j, i in
+        // the row's own token) is summed apart: its contributions to dPhi through B~ and
+        // C~ cancel exactly (C~_i . B~_j is unchanged by a common rotation), so dPhi is
+        // formed from the other terms alone, free of that cancellation.  So is the s-term
+        // of the last token's rows in the last chunk (its pair with the final state).
+        const bool last = (c == nch - 1);
+        for (int e = tid; e < QR * K; e += kThreads) {
+            const int i = e / K, k = e % K, ti = i / R;
+            const int n0 = 2 * k;
+            float c_off[2] = {0.0f, 0.0f}, c_dg[2] = {0.0f, 0.0f}, b_off[2] = {0.0f, 0.0f}, b_dg[2] = {0.0f, 0.0f};
+            float b_s[2];
+            for (int j = 0; j < ti * R; ++j) {
+                const float d = dS[i * QS + j];
+                c_off[0] = fmaf(d, Bt[j * NS + n0], c_off[0]);
+                c_off[1] = fmaf(d, Bt[j * NS + n0 + 1], c_off[1]);
+            }
+            for (int j = ti * R; j < (ti + 1) * R; ++j) {
+                const float d = dS[i * QS + j];
+                c_dg[0] = fmaf(d, Bt[j * NS + n0], c_dg[0]);
+                c_dg[1] = fmaf(d, Bt[j * NS + n0 + 1], c_dg[1]);
+                const float d2 = dS[j * QS + i];
+                b_dg[0] = fmaf(d2, Ct[j * NS + n0], b_dg[0]);
+                b_dg[1] = fmaf(d2, Ct[j * NS + n0 + 1], b_dg[1]);
+            }
+            for (int i2 = (ti + 1) * R; i2 < QR; ++i2) {
+                const float d = dS[i2 * QS + i];
+                b_off[0] = fmaf(d, Ct[i2 * NS + n0], b_off[0]);
+                b_off[1] = fmaf(d, Ct[i2 * NS + n0 + 1], b_off[1]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                c_off[u] = fmaf(ecs[ti], T2[i * NS + n0 + u], c_off[u]);
+                b_s[u] = sv[ti] * XG[i * NS + n0 + u];
+            }
+            if (theta) {
+                // this row's share of dPhi_t[k]: d/dPhi Rot(-Phi) v = (v~_1, -v~_0)
+                const float sterm = b_s[0] * Bt[i * NS + n0 + 1] - b_s[1] * Bt[i * NS + n0];
+                const bool fin = last && ti == nt - 1;
+                dpr[i * K + k] = b_off[0] * Bt[i * NS + n0 + 1] - b_off[1] * Bt[i * NS + n0] +
+                                 c_off[0] * Ct[i * NS + n0 + 1] - c_off[1] * Ct[i * NS + n0] + (fin ? 0.0f : sterm);
+                if (last) spr[i * K + k] = (fin || ti >= nt) ? 0.0f : sterm;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                T2[i * NS + n0 + u] = c_off[u] + c_dg[u];
+                XG[i * NS + n0 + u] = b_off[u] + b_s[u] + b_dg[u];
+            }
         }
         // ---- (6) token scalars (warp 0): dcs, dw, dgamma from dM, exp(cs), s and <dG, G>
         if (tid < 32) {
@@ -494,32 +549,36 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
                     }
                     // exp(cs_t) of the inter-chunk output; s_t = exp(cs_end - cs_t) w_t of the state update
                     a_cs = fmaf(ebar[i], ecs[t], a_cs);
-                    a_cs = fmaf(-dsr[i], sv[t], a_cs);
                     a_w = fmaf(dsr[i], expf(cs_end - cs[t]), a_w);
                 }
+                // s_t = exp(cs_end - cs_t) w_t depends on dt_k for t < k <= end only: its
+                // term x_t is added over that range below rather than as + at cs_end and
+                // - at cs_t (which would cancel, inexactly, for every k <= t)
+                float x = 0.0f;
+                for (int r = 0; r < R; ++r) x = fmaf(dsr[t * R + r], sv[t], x);
+                xs[t] = x;
                 dcs[t] = a_cs;
                 dw[t] = a_w;
                 dgm[t] = a_g;
             }
-            // cs_end: through exp(cs_end) G_{c-1} and through every s_t
-            float part = 0.0f;
-            for (int i = tid; i < QR; i += 32) part = fmaf(dsr[i], sv[i / R], part);
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             __syncwarp();
             if (tid == 0) {
-                dcs[Q - 1] += part + red[kThreads] * expf(cs_end);
-                // cs_t = A sum_{k <= t} dt_k:  ddt_k += A sum_{t >= k} dcs_t,  dA += sum_t dcs_t sum_{k <= t} dt_k
-                float run = 0.0f, dA_c = 0.0f;
+                dcs[Q - 1] += red[kThreads] * expf(cs_end);   // cs_end through exp(cs_end) G_{c-1}
+                // cs_t = A sum_{k <= t} dt_k:  with R_k = sum_{t >= k} dcs_t + sum_{t < k} x_t,
+                // ddt_k += A R_k and dA += sum_k dt_k R_k
+                float pre = 0.0f;
                 for (int t = 0; t < Q; ++t) {
-                    run += s_dt[t];
-                    dA_c = fmaf(dcs[t], run, dA_c);
+                    csdt[t] = pre;                       // sum_{t' < t} x_t'
+                    pre += xs[t];
                 }
-                pend[2] += dA_c;
-                float suf = 0.0f;
+                float suf = 0.0f, dA_c = 0.0f;
                 for (int t = Q - 1; t >= 0; --t) {
                     suf += dcs[t];
-                    csdt[t] = A_h * suf;                 // ddt_t through cs
+                    const float Rk = suf + csdt[t];
+                    dA_c = fmaf(s_dt[t], Rk, dA_c);
+                    csdt[t] = A_h * Rk;                  // ddt_t through cs
                 }
+                pend[2] += dA_c;
                 // w_t = gamma_t + (1 - lambda_{t+1}) dt_{t+1};  gamma_t = lambda_t dt_t
                 float nd = 0.0f, nl = 0.0f;               // w_{Q-1}'s part for token c0 + Q
                 for (int t = Q - 1; t >= 0; --t) {
@@ -557,7 +616,7 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
             }
         }
         __syncthreads();
-        // ---- (7) rotation: every row's share of dPhi per pair, dB, dC rotated back;
+        // ---- (7) rotation: dB, dC rotated back (dPhi was formed in (5));
         //      dtheta = suffix sums (thread per pair)
         if (theta) {
             for (int e = tid; e < QR * K; e += kThreads) {
@@ -568,14 +627,17 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
                 // dB = Rot(+Phi) dB~, dC likewise
                 const float ob0 = fmaf(db0, cn, -db1 * sn), ob1 = fmaf(db0, sn, db1 * cn);
                 const float oc0 = fmaf(dc0, cn, -dc1 * sn), oc1 = fmaf(dc0, sn, dc1 * cn);
-                // this row's share of dPhi_t[k]: d/dPhi Rot(-Phi) v = (v~_1, -v~_0)
-                const float dp = db0 * Bt[i0 + 1] - db1 * Bt[i0] + dc0 * Ct[i0 + 1] - dc1 * Ct[i0];
                 XG[i0] = ob0; XG[i0 + 1] = ob1; T2[i0] = oc0; T2[i0 + 1] = oc1;
-                dpr[row * K + k] = dp;
             }
             __syncthreads();
             for (int k = tid; k < K; k += kThreads) {
                 float acc = dphi_c[k];
+                if (c == nch - 1) {
+                    // the final state's angle term: through G_{nch-1}, decayed over the chunk,
+                    // and through the chunk's rows but the last token's
+                    acc *= expf(cs[Q - 1]);
+                    for (int i = 0; i < QR; ++i) acc -= spr[i * K + k];
+                }
                 for (int t = Q - 1; t >= 0; --t) {
                     float v = 0.0f;
                     for (int r = 0; r < R; ++r) v += dpr[(t * R + r) * K + k];

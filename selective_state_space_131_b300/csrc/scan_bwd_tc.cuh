@@ -68,7 +68,8 @@ constexpr int F_PHI0 = F_DPHI + 32;                                             
 constexpr int F_DTOK = F_PHI0 + 32;                                                      // [2][64] ddt, dlam of the chunk
 constexpr int F_CZM = F_DTOK + 128, F_CZE = F_CZM + 64;                                  // per column
 constexpr int F_SEG = F_CZE + 64;                                                        // [4][32] segment totals
-constexpr int F_END = F_SEG + 128;
+constexpr int F_DSD = F_SEG + 128;                                                       // [64][4] dS, same-token block
+constexpr int F_END = F_DSD + 256;
 constexpr int OFF_GB = (OFF_F + F_END * 4 + 1023) & ~1023;   // fp32 G checkpoint, 2 stages x [64][64]
 constexpr int SMEM_BYTES = OFF_GB + 2 * 64 * 64 * 4 + 1024;
 // TMEM columns
@@ -243,7 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // dG_last = Rot(-Phi_{T-1}) dfinal, held in fp32 by warpgroup 0 (rows n =
     // `row`, columns 32 hc ..); the final rotation's angle gradient
-    // sum_p (-df_0 f_1 + df_1 f_0), f = Rot(Phi) G_last, starts the dtheta carry
+    // sum_p (-df_0 f_1 + df_1 f_0), f = Rot(Phi) G_last, starts the dtheta carry.  Here
+    // its part through G_{nch-1} (f = Rot(Phi) G_{nch-1}); the last chunk decays it and
+    // adds the part through its own rows
     float dG[32];
     const int64_t ckb = (int64_t)unit * (nch + 1);
     if (tid < 32) F[F_DPHI + tid] = 0.0f;
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = 0; p < 32; ++p) {
             const float df = prm.dfinal ? __ldg(prm.dfinal + ((int64_t)unit * 64 + row) * 64 + 32 * hc + p) : 0.0f;
             const float dfo = __shfl_xor_sync(0xffffffffu, df, 1);   // the pair partner's row
-            const float g = __ldg(prm.ck_G + ((ckb + nch) * 64 + row) * 64 + 32 * hc + p);
+            const float g = __ldg(prm.ck_G + ((ckb + nch - 1) * 64 + row) * 64 + 32 * hc + p);
             const float go = __shfl_xor_sync(0xffffffffu, g, 1);
             // Rot(-phi) (df0, df1) = (df0 c + df1 s, -df0 s + df1 c)
             dG[p] = even ? fmaf(df, cn, dfo * sn) : fmaf(-dfo, sn, df * cn);
@@ -367,7 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cs[u] = a;
             }
             cs[1] += __shfl_sync(0xffffffffu, cs[0], 31);
-            const float cs_end = (Q == 64) ? __shfl_sync(0xffffffffu, cs[1], 31) : __shfl_sync(0xffffffffu, cs[0], Q - 1);
+            // cs_end is the last valid token's cs, and past it (dt = 0) cs repeats that
+            // value bit for bit, so that 2^(cs_end - cs) is exactly 1 for the last token
+            const int lt = nt - 1;   // uniform over the warp
+            const float cs_end = __shfl_sync(0xffffffffu, (lt < 32) ? cs[0] : cs[1], lt & 31);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (u * 32 + lane > lt) cs[u] = cs_end;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = u * 32 + lane;
@@ -511,7 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = gam_i;
                 }
                 sp[e] = S * m;
-                ds[e] = dSp * m;
+                // the tile takes dS without the same-token block, which epilogue 2 adds in
+                // fp32 (so that dPhi can be formed without it)
+                ds[e] = (tj == ti) ? 0.0f : dSp * m;
+                if (tj == ti) F[F_DSD + row * 4 + (j - ti * R)] = dSp * m;
                 const float z = dSp * S;
                 const float zmv = (tj < ti) ? z * m : 0.0f;
                 rzm += zmv;
@@ -553,6 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 F[F_EBAR + row] = eb;
                 F[F_DSR + row] = dsr;
             }
+            if (c == nch - 1 && prm.theta) {
+                // last chunk: this row's s-term share of dPhi, i.e. minus its pair with the
+                // final state, for the start of the dtheta sum (the last token's rows
+                // excluded: that pair has zero angle); nothing reads F_DPR yet
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    F[F_DPR + row * KS + 16 * hc + m] =
+                        (t >= nt - 1) ? 0.0f : sX[2 * m] * br[2 * m + 1] - sX[2 * m + 1] * br[2 * m];
+            }
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
@@ -591,41 +612,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             F[(tid < 192 ? F_CZM : F_CZE) + j] = a0 + a1;
             ptx::bar_sync(2, 128);
             if (warp >= 6 && prm.theta && c + 1 < nch) dtheta_chunk(c + 1);
+            if (warp == 6 && prm.theta && c == nch - 1) {
+                // the final state's angle term: the part through G_{nch-1}, decayed over
+                // the chunk, and the part through the chunk's rows but the last token's
+                float acc = F[F_DPHI + lane] * m3::ex2_approx(F[F_CS + Q - 1]);
+                for (int r2 = 0; r2 < 64; ++r2) acc -= F[F_DPR + r2 * KS + lane];
+                F[F_DPHI + lane] = acc;
+            }
         }
         if (warp == 4) {
             const float cs_end = F[F_CS + Q - 1];
             const float gdot = F[F_RED] + F[F_RED + 1] + F[F_RED + 2] + F[F_RED + 3];
-            // per token (lane: tokens lane, lane + 32): dcs, dw, dgamma
-            float dcs[2], dw[2], dg[2];
-            float part = 0.0f;
+            // per token (lane: tokens lane, lane + 32): dcs, dw, dgamma; x_t, the gradient
+            // of s_t = exp(cs_end - cs_t) w_t through its decay, which depends on dt_k for
+            // t < k <= end only: it is added over that range (R_k below) rather than as +
+            // at cs_end and - at cs_t, which would cancel, inexactly, for every k <= t
+            float dcs[2], dw[2], dg[2], xs[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = u * 32 + lane;
-                dcs[u] = 0.0f; dw[u] = 0.0f; dg[u] = 0.0f;
+                dcs[u] = 0.0f; dw[u] = 0.0f; dg[u] = 0.0f; xs[u] = 0.0f;
                 if (t < Q) {
                     const float s_t = F[F_S + t], ecs_t = F[F_ECS + t], ee = F[F_EEND + t];
                     for (int r = 0; r < R; ++r) {
                         const int i = t * R + r;
-                        dcs[u] += F[F_RZM + i] - F[F_CZM + i] + F[F_EBAR + i] * ecs_t - F[F_DSR + i] * s_t;
+                        dcs[u] += F[F_RZM + i] - F[F_CZM + i] + F[F_EBAR + i] * ecs_t;
                         dw[u] += F[F_CZE + i] + F[F_DSR + i] * ee;
                         dg[u] += F[F_RG + i];
-                        part = fmaf(F[F_DSR + i], s_t, part);
+                        xs[u] = fmaf(F[F_DSR + i], s_t, xs[u]);
                     }
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            // cs_end: through exp(cs_end) G_{c-1} and every s_t (cs here in log2 units;
-            // the gradients are with respect to the natural-log cs: d/dcs 2^(x log2 e) = value)
-            const float dcs_end = part + gdot * m3::ex2_approx(cs_end);
+            // cs_end: through exp(cs_end) G_{c-1} (cs here in log2 units; the gradients are
+            // with respect to the natural-log cs: d/dcs 2^(x log2 e) = value)
+            const float dcs_end = gdot * m3::ex2_approx(cs_end);
             if (Q == 64) { if (lane == 31) dcs[1] += dcs_end; }
             else if (lane == Q - 1) dcs[0] += dcs_end;
-            // ddt through cs: A sum_{t' >= t} dcs_t'; dA: sum_t dcs_t sum_{k <= t} dt_k
+            // R_k = sum_{t >= k} dcs_t + sum_{t < k} x_t;  ddt_k += A R_k;  dA += sum_k dt_k R_k
             const float* sdt = F + F_DL + st * 2 * 68;
             const float* slm = sdt + 68;
             float sfx[2];
             {
-                // suffix sums over the 64 tokens (lane u * 32 + lane)
+                // suffix sums of dcs over the 64 tokens (lane u * 32 + lane)
                 float a1 = dcs[1];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -640,23 +668,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 sfx[1] = a1;
                 sfx[0] = a0 + __shfl_sync(0xffffffffu, a1, 0);
+                // exclusive prefix sums of x
+                float p0 = xs[0], p1 = xs[1];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float v0 = __shfl_up_sync(0xffffffffu, p0, o);
+                    const float v1 = __shfl_up_sync(0xffffffffu, p1, o);
+                    if (lane >= o) { p0 += v0; p1 += v1; }
+                }
+                // exclusive: the previous lane's inclusive sum (never "inclusive - own",
+                // which cancels against an x of much larger size)
+                const float tot0 = __shfl_sync(0xffffffffu, p0, 31);
+                const float e0 = __shfl_up_sync(0xffffffffu, p0, 1), e1 = __shfl_up_sync(0xffffffffu, p1, 1);
+                sfx[0] += (lane == 0) ? 0.0f : e0;
+                sfx[1] += (lane == 0) ? tot0 : tot0 + e1;
             }
             float dA_c = 0.0f;
             {
-                float pre[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int t = u * 32 + lane;
-                    float a = (t < Q) ? sdt[t] : 0.0f;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float v = __shfl_up_sync(0xffffffffu, a, o);
-                        if (lane >= o) a += v;
-                    }
-                    pre[u] = a;
+                    if (t < Q) dA_c = fmaf(sdt[t], sfx[u], dA_c);
                 }
-                pre[1] += __shfl_sync(0xffffffffu, pre[0], 31);
-                dA_c = dcs[0] * pre[0] + dcs[1] * pre[1];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dA_c += __shfl_xor_sync(0xffffffffu, dA_c, o);
             }
@@ -751,12 +784,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             float cr[32], br[32];
             tile_row32(sbase + ST_C, row, hc, cr);
             tile_row32(sbase + ST_B, row, hc, br);
+            // the same-token block's share of dC~ (row i: sum over j in i's token of
+            // dS_ij B~_j) and of dB~ (row j: sum over i in j's token of dS_ij C~_i), in
+            // fp32 (the products above left it out): its contributions to dPhi through
+            // B~ and C~ cancel exactly (C~_i . B~_j is unchanged by a common rotation), so
+            // dPhi is formed without it, free of that cancellation.  Likewise the s-term
+            // of the last token's rows in the last chunk (its pair with the final state).
+            float cdg[32], bdg[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) { cdg[e] = 0.0f; bdg[e] = 0.0f; }
+            {
+                for (int r = 0; r < R; ++r) {
+                    const int o = t * R + r;   // a row of the same token
+                    const float d_io = F[F_DSD + row * 4 + r], d_oi = F[F_DSD + o * 4 + (row - t * R)];
+                    float vb2[32], vc2[32];
+                    tile_row32(sbase + ST_B, o, hc, vb2);
+                    tile_row32(sbase + ST_C, o, hc, vc2);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        cdg[e] = fmaf(d_io, vb2[e], cdg[e]);
+                        bdg[e] = fmaf(d_oi, vc2[e], bdg[e]);
+                    }
+                }
+            }
+            const bool fin = (c == nch - 1) && t == nt - 1;
             float oc[32], ob[32];
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int k = 16 * hc + m;
-                const float dc0 = __uint_as_float(vc[2 * m]) + eT[2 * m], dc1 = __uint_as_float(vc[2 * m + 1]) + eT[2 * m + 1];
-                const float db0 = __uint_as_float(vb[2 * m]) + sX[2 * m], db1 = __uint_as_float(vb[2 * m + 1]) + sX[2 * m + 1];
+                // f: the terms that enter dPhi; d: the whole dC~ / dB~
+                const float fc0 = __uint_as_float(vc[2 * m]) + eT[2 * m], fc1 = __uint_as_float(vc[2 * m + 1]) + eT[2 * m + 1];
+                const float vb0 = __uint_as_float(vb[2 * m]), vb1 = __uint_as_float(vb[2 * m + 1]);
+                const float fb0 = fin ? vb0 : vb0 + sX[2 * m], fb1 = fin ? vb1 : vb1 + sX[2 * m + 1];
+                const float dc0 = fc0 + cdg[2 * m], dc1 = fc1 + cdg[2 * m + 1];
+                const float db0 = vb0 + sX[2 * m] + bdg[2 * m], db1 = vb1 + sX[2 * m + 1] + bdg[2 * m + 1];
                 float co = 1.0f, si = 0.0f;
                 if (prm.theta) { co = F[F_COS + t * KS + k]; si = F[F_SIN + t * KS + k]; }
                 // dB = Rot(+phi) dB~: (a cos - b sin, a sin + b cos)
@@ -765,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ob[2 * m] = fmaf(db0, co, -db1 * si);
                 ob[2 * m + 1] = fmaf(db0, si, db1 * co);
                 // d/dphi Rot(-phi) v = (v~_1, -v~_0)
-                F[F_DPR + row * KS + k] = db0 * br[2 * m + 1] - db1 * br[2 * m] + dc0 * cr[2 * m + 1] - dc1 * cr[2 * m];
+                F[F_DPR + row * KS + k] = fb0 * br[2 * m + 1] - fb1 * br[2 * m] + fc0 * cr[2 * m + 1] - fc1 * cr[2 * m];
             }
             if (t < nt) {
                 const int64_t gi = (tok_idx(t0 + t) * R + (row - t * R)) * 64 + 32 * hc;

@@ -191,6 +191,11 @@ __global__ void __launch_bounds__(kThreads) m3_scan_chunk_kernel(
                 }
             }
             __syncwarp();
+            // past the end (dt = 0) cs stays at the last token's value -- bit for bit, so
+            // that exp(cs_end - cs) is exactly 1 there, as the scan's rounding would not
+            // guarantee
+            for (int t = nt + lane; t < Q; t += 32) sc_cs[t] = sc_cs[nt - 1];
+            __syncwarp();
             const float cs_end = sc_cs[Q - 1];
             for (int t = lane; t < Q; t += 32) {
                 const float gam = s_lam[t] * s_dt[t];
