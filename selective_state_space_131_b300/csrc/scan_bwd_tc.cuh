@@ -117,6 +117,24 @@ __device__ __forceinline__ void tile_row32(const uint8_t* t, int row, int hc, fl
         }
     }
 }
+// the 8 columns of 16-byte group gg of row `row` of a tile as floats
+__device__ __forceinline__ void tile_row8(const uint8_t* t, int row, int gg, float (&o)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(t + swz(row, gg));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        o[2 * m] = lo16(u[m]);
+        o[2 * m + 1] = hi16(u[m]);
+    }
+}
+// 16 columns: 16-byte groups gg, gg + 1 of row `row`
+__device__ __forceinline__ void tile_put16(uint8_t* t, int row, int gg, const float (&v)[16]) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+        *reinterpret_cast<uint4*>(t + swz(row, gg + g)) =
+            make_uint4(pack2(v[8 * g], v[8 * g + 1]), pack2(v[8 * g + 2], v[8 * g + 3]),
+                       pack2(v[8 * g + 4], v[8 * g + 5]), pack2(v[8 * g + 6], v[8 * g + 7]));
+}
 __device__ __forceinline__ void tile_put32(uint8_t* t, int row, int hc, const float (&v)[32]) {
 #pragma unroll
     for (int g = 0; g < 4; ++g)
@@ -499,37 +517,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         float eT[32];     // warpgroup 1: exp(cs_i) T2 (row i) or s_j XG (row j), kept for (6)
         float sX[32];
         if (wg == 0) {
-            // S, dS' of row i, columns 32 hc ..: mask, S', dS, dM
-            uint32_t vs[32], vd[32];
-            ptx::tmem_ld16x2_32(tmem + lane_base + TM_S, vs);
-            ptx::tmem_ld16x2_32(tmem + lane_base + TM_DSP, vd);
-            ptx::tmem_ld_wait();
+            // S, dS' of row i, columns 32 hc ..: mask, S', dS, dM -- in two halves of 16
+            // columns, to keep the registers in bounds
             const int ti = row / R;
             const float cs_i = F[F_CS + ti], gam_i = F[F_GAM + ti];
-            float sp[32], ds[32];
             float rzm = 0.0f, rg = 0.0f;
+            float dsd[R];   // dS of the same-token block (selected, no dynamic register index)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int j = 32 * hc + e, tj = j / R;
-                const float S = __uint_as_float(vs[e]), dSp = __uint_as_float(vd[e]);
-                float m = 0.0f, ez = 0.0f;
-                if (tj < ti) {
-                    ez = m3::ex2_approx(cs_i - F[F_CS + tj]);
-                    m = ez * F[F_W + tj];
-                } else if (tj == ti) {
-                    m = gam_i;
+            for (int r = 0; r < R; ++r) dsd[r] = 0.0f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t vs[16], vd[16];
+                ptx::tmem_ld16x2_16(tmem + lane_base + TM_S + 16 * half, vs);
+                ptx::tmem_ld16x2_16(tmem + lane_base + TM_DSP + 16 * half, vd);
+                ptx::tmem_ld_wait();
+                float sp[16], ds[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int j = 32 * hc + 16 * half + e, tj = j / R;
+                    const float S = __uint_as_float(vs[e]), dSp = __uint_as_float(vd[e]);
+                    float m = 0.0f, ez = 0.0f;
+                    if (tj < ti) {
+                        ez = m3::ex2_approx(cs_i - F[F_CS + tj]);
+                        m = ez * F[F_W + tj];
+                    } else if (tj == ti) {
+                        m = gam_i;
+                    }
+                    sp[e] = S * m;
+                    // the tile takes dS without the same-token block, which epilogue 2 adds
+                    // in fp32 (so that dPhi can be formed without it)
+                    ds[e] = (tj == ti) ? 0.0f : dSp * m;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) dsd[r] += (j == ti * R + r) ? dSp * gam_i : 0.0f;
+                    const float z = dSp * S;
+                    const float zmv = (tj < ti) ? z * m : 0.0f;
+                    rzm += zmv;
+                    if (tj == ti) rg += z;
+                    zm[row * 65 + j] = zmv;
+                    ze[row * 65 + j] = (tj < ti) ? z * ez : 0.0f;
                 }
-                sp[e] = S * m;
-                // the tile takes dS without the same-token block, which epilogue 2 adds in
-                // fp32 (so that dPhi can be formed without it)
-                ds[e] = (tj == ti) ? 0.0f : dSp * m;
-                if (tj == ti) F[F_DSD + row * 4 + (j - ti * R)] = dSp * m;
-                const float z = dSp * S;
-                const float zmv = (tj < ti) ? z * m : 0.0f;
-                rzm += zmv;
-                if (tj == ti) rg += z;
-                zm[row * 65 + j] = zmv;
-                ze[row * 65 + j] = (tj < ti) ? z * ez : 0.0f;
+                tile_put16(smem + OFF_SP, row, 4 * hc + 2 * half, sp);
+                tile_put16(smem + OFF_DS, row, 4 * hc + 2 * half, ds);
             }
             rzm += __shfl_xor_sync(0xffffffffu, rzm, 16);
             rg += __shfl_xor_sync(0xffffffffu, rg, 16);
@@ -537,8 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 F[F_RZM + row] = rzm;
                 F[F_RG + row] = rg;
             }
-            tile_put32(smem + OFF_SP, row, hc, sp);
-            tile_put32(smem + OFF_DS, row, hc, ds);
+            if ((ti * R) / 32 == hc) {   // the block lies in this thread's column half
+#pragma unroll
+                for (int r = 0; r < R; ++r) F[F_DSD + row * 4 + r] = dsd[r];
+            }
         } else {
             // T2 (row i: ebar_i = C~_i . T2_i) and XG (row j: ds_j = B~_j . XG_j)
             uint32_t vt[32], vx[32];
@@ -781,63 +811,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld16x2_32(tmem + lane_base + TM_DB, vb);
             ptx::tmem_ld_wait();
             const int t = row / R;
-            float cr[32], br[32];
-            tile_row32(sbase + ST_C, row, hc, cr);
-            tile_row32(sbase + ST_B, row, hc, br);
             // the same-token block's share of dC~ (row i: sum over j in i's token of
             // dS_ij B~_j) and of dB~ (row j: sum over i in j's token of dS_ij C~_i), in
             // fp32 (the products above left it out): its contributions to dPhi through
             // B~ and C~ cancel exactly (C~_i . B~_j is unchanged by a common rotation), so
             // dPhi is formed without it, free of that cancellation.  Likewise the s-term
             // of the last token's rows in the last chunk (its pair with the final state).
-            float cdg[32], bdg[32];
+            // Eight columns (four pairs) at a time, to keep the registers in bounds.
+            float d_io[R], d_oi[R];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) { cdg[e] = 0.0f; bdg[e] = 0.0f; }
-            {
-                for (int r = 0; r < R; ++r) {
-                    const int o = t * R + r;   // a row of the same token
-                    const float d_io = F[F_DSD + row * 4 + r], d_oi = F[F_DSD + o * 4 + (row - t * R)];
-                    float vb2[32], vc2[32];
-                    tile_row32(sbase + ST_B, o, hc, vb2);
-                    tile_row32(sbase + ST_C, o, hc, vc2);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        cdg[e] = fmaf(d_io, vb2[e], cdg[e]);
-                        bdg[e] = fmaf(d_oi, vc2[e], bdg[e]);
-                    }
-                }
+            for (int r = 0; r < R; ++r) {
+                d_io[r] = F[F_DSD + row * 4 + r];
+                d_oi[r] = F[F_DSD + (t * R + r) * 4 + (row - t * R)];
             }
             const bool fin = (c == nch - 1) && t == nt - 1;
-            float oc[32], ob[32];
+            const int64_t gi = (tok_idx(t0 + t) * R + (row - t * R)) * 64 + 32 * hc;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int k = 16 * hc + m;
-                // f: the terms that enter dPhi; d: the whole dC~ / dB~
-                const float fc0 = __uint_as_float(vc[2 * m]) + eT[2 * m], fc1 = __uint_as_float(vc[2 * m + 1]) + eT[2 * m + 1];
-                const float vb0 = __uint_as_float(vb[2 * m]), vb1 = __uint_as_float(vb[2 * m + 1]);
-                const float fb0 = fin ? vb0 : vb0 + sX[2 * m], fb1 = fin ? vb1 : vb1 + sX[2 * m + 1];
-                const float dc0 = fc0 + cdg[2 * m], dc1 = fc1 + cdg[2 * m + 1];
-                const float db0 = vb0 + sX[2 * m] + bdg[2 * m], db1 = vb1 + sX[2 * m + 1] + bdg[2 * m + 1];
-                float co = 1.0f, si = 0.0f;
-                if (prm.theta) { co = F[F_COS + t * KS + k]; si = F[F_SIN + t * KS + k]; }
-                // dB = Rot(+phi) dB~: (a cos - b sin, a sin + b cos)
-                oc[2 * m] = fmaf(dc0, co, -dc1 * si);
-                oc[2 * m + 1] = fmaf(dc0, si, dc1 * co);
-                ob[2 * m] = fmaf(db0, co, -db1 * si);
-                ob[2 * m + 1] = fmaf(db0, si, db1 * co);
-                // d/dphi Rot(-phi) v = (v~_1, -v~_0)
-                F[F_DPR + row * KS + k] = fb0 * br[2 * m + 1] - fb1 * br[2 * m] + fc0 * cr[2 * m + 1] - fc1 * cr[2 * m];
-            }
-            if (t < nt) {
-                const int64_t gi = (tok_idx(t0 + t) * R + (row - t * R)) * 64 + 32 * hc;
+            for (int g = 0; g < 4; ++g) {
+                float cr[8], br[8], cdg[8], bdg[8];
+                tile_row8(sbase + ST_C, row, 4 * hc + g, cr);
+                tile_row8(sbase + ST_B, row, 4 * hc + g, br);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    reinterpret_cast<uint4*>(prm.dC + gi)[g] =
-                        make_uint4(pack2(oc[8 * g], oc[8 * g + 1]), pack2(oc[8 * g + 2], oc[8 * g + 3]),
-                                   pack2(oc[8 * g + 4], oc[8 * g + 5]), pack2(oc[8 * g + 6], oc[8 * g + 7]));
-                    reinterpret_cast<uint4*>(prm.dB + gi)[g] =
-                        make_uint4(pack2(ob[8 * g], ob[8 * g + 1]), pack2(ob[8 * g + 2], ob[8 * g + 3]),
-                                   pack2(ob[8 * g + 4], ob[8 * g + 5]), pack2(ob[8 * g + 6], ob[8 * g + 7]));
+                for (int e = 0; e < 8; ++e) { cdg[e] = 0.0f; bdg[e] = 0.0f; }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float vb2[8], vc2[8];
+                    tile_row8(sbase + ST_B, t * R + r, 4 * hc + g, vb2);
+                    tile_row8(sbase + ST_C, t * R + r, 4 * hc + g, vc2);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        cdg[e] = fmaf(d_io[r], vb2[e], cdg[e]);
+                        bdg[e] = fmaf(d_oi[r], vc2[e], bdg[e]);
+                    }
+                }
+                uint32_t pc[4], pb[4];
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const int m = 4 * g + mm, k = 16 * hc + m, e = 2 * mm;
+                    // f: the terms that enter dPhi; d: the whole dC~ / dB~
+                    const float fc0 = __uint_as_float(vc[2 * m]) + eT[2 * m];
+                    const float fc1 = __uint_as_float(vc[2 * m + 1]) + eT[2 * m + 1];
+                    const float vb0 = __uint_as_float(vb[2 * m]), vb1 = __uint_as_float(vb[2 * m + 1]);
+                    const float fb0 = fin ? vb0 : vb0 + sX[2 * m], fb1 = fin ? vb1 : vb1 + sX[2 * m + 1];
+                    const float dc0 = fc0 + cdg[e], dc1 = fc1 + cdg[e + 1];
+                    const float db0 = vb0 + sX[2 * m] + bdg[e], db1 = vb1 + sX[2 * m + 1] + bdg[e + 1];
+                    float co = 1.0f, si = 0.0f;
+                    if (prm.theta) { co = F[F_COS + t * KS + k]; si = F[F_SIN + t * KS + k]; }
+                    // dC = Rot(+phi) dC~, dB likewise: (a cos - b sin, a sin + b cos)
+                    pc[mm] = pack2(fmaf(dc0, co, -dc1 * si), fmaf(dc0, si, dc1 * co));
+                    pb[mm] = pack2(fmaf(db0, co, -db1 * si), fmaf(db0, si, db1 * co));
+                    // d/dphi Rot(-phi) v = (v~_1, -v~_0)
+                    F[F_DPR + row * KS + k] = fb0 * br[e + 1] - fb1 * br[e] + fc0 * cr[e + 1] - fc1 * cr[e];
+                }
+                if (t < nt) {
+                    reinterpret_cast<uint4*>(prm.dC + gi)[g] = make_uint4(pc[0], pc[1], pc[2], pc[3]);
+                    reinterpret_cast<uint4*>(prm.dB + gi)[g] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
                 }
             }
         }
