@@ -48,6 +48,9 @@ NCU_TRAFFIC = {
     "decode_f32_b256h32P64N64_R1": {"bytes": 145.835264e6 + 77.099520e6,
                                     "source": "selective_state_space_131_b300/csrc/step_fast.cuh",
                                     "sha256": "dcdb0919045c3efd"},
+    "decode_f32_b256h32P64N64_R4": {"bytes": 177.312768e6 + 84.965120e6,
+                                    "source": "selective_state_space_131_b300/csrc/step_ring.cuh",
+                                    "sha256": "8cd37f266fbcedb5"},
 }
 
 

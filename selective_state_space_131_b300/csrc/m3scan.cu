@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "step_simt.cuh"
 #include "step_fast.cuh"
+#include "step_ring.cuh"
 #include "scan_ws.cuh"
 #include "scan_chunk.cuh"
 #include "scan_bwd.cuh"
@@ -187,6 +188,43 @@ int launch_step_fast(const m3_dims* d, float* state, const void* x_t, const floa
         default: return M3_ERR_UNSUPPORTED;
     }
 #undef M3_STEP_FAST
+    return launch_status();
+}
+
+// The decode step through the shared-memory ring (step_ring.cuh): persistent
+// CTAs, as many as fit on the device at once; every tensor is 16-byte aligned
+// and every per-unit block a multiple of 16 bytes (checked by the caller).
+template <typename T>
+int launch_step_ring(const m3_dims* d, float* state, const void* x_t, const float* dt_t, const float* A,
+                     const void* B_t, const void* C_t, const float* lam_t, const void* theta_t, const void* prev_B,
+                     const void* prev_x, void* y_t, cudaStream_t s) {
+    const m3ring::Geo g = m3ring::make_geo(d->batch * d->heads, (int)d->heads, (int)d->dstate, (int)d->headdim,
+                                           (int)d->rank, (int)sizeof(T));
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return M3_ERR_CUDA;
+    int rc = M3_OK;
+#define M3_STEP_RING(RR, MT)                                                                                    \
+    do {                                                                                                        \
+        auto k = m3ring::m3_step_ring_kernel<T, RR, MT>;                                                        \
+        rc = prepare(k, g.smem_bytes);                                                                          \
+        if (rc != M3_OK) return rc;                                                                             \
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, g.nthreads, g.smem_bytes) != cudaSuccess || \
+            per_sm < 1)                                                                                         \
+            return M3_ERR_UNSUPPORTED;                                                                          \
+        const int64_t want = (int64_t)sms * per_sm;                                                             \
+        const unsigned grid = (unsigned)(g.units < want ? g.units : want);                                      \
+        k<<<grid, g.nthreads, g.smem_bytes, s>>>(g, state, (const T*)x_t, dt_t, A, (const T*)B_t, (const T*)C_t,   \
+                                                lam_t, (const T*)theta_t, (const T*)prev_B, (const T*)prev_x,      \
+                                                (T*)y_t);                                                       \
+    } while (0)
+    const bool small = g.nthreads <= 128;
+    switch (d->rank) {
+        case 2: if (small) M3_STEP_RING(2, 128); else M3_STEP_RING(2, 256); break;
+        case 4: if (small) M3_STEP_RING(4, 128); else M3_STEP_RING(4, 256); break;
+        default: return M3_ERR_UNSUPPORTED;
+    }
+#undef M3_STEP_RING
     return launch_status();
 }
 
@@ -512,6 +550,12 @@ int m3_step(const m3_dims* d, float* state, const void* x_t, const float* dt_t, 
         if (ok16) {
             if (d->batch == 0) return M3_OK;
             cudaStream_t s = static_cast<cudaStream_t>(stream);
+            if (m3ring::supports(d->dstate, d->headdim, d->rank, (int)es))
+                return d->dtype == M3_F32
+                           ? launch_step_ring<float>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B,
+                                                     prev_x, y_t, s)
+                           : launch_step_ring<__nv_bfloat16>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t,
+                                                             prev_B, prev_x, y_t, s);
             return d->dtype == M3_F32
                        ? launch_step_fast<float>(d, state, x_t, dt_t, A, B_t, C_t, lambda_t, theta_t, prev_B, prev_x,
                                                  y_t, s)

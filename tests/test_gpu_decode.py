@@ -194,3 +194,13 @@ def test_decode_sweep_1024_steps_in_graph(m3, R):
         worst = (max(worst[0], ey), max(worst[1], es))
         assert ey <= 1e-4 and es <= 1e-4, (k, ey, es)
     print(f"R{R} 1024 steps: worst segment y {worst[0]:.2e} state {worst[1]:.2e}")
+
+
+@pytest.mark.parametrize("R,dtype", [(4, "f32"), (1, "bf16")])
+def test_decode_step_every_unit(m3, R, dtype):
+    """One decode step of b256 h32 P64 N64 checked on every (batch, head) unit:
+    the persistent kernel walks many units per CTA, so an indexing mistake would
+    show on some units only."""
+    shape = inputs.DecodeShape(batch=256, heads=32, headdim=64, dstate=64, rank=R, steps=2, dtype=dtype)
+    ey, es = run_chain(m3, shape, 300 + R, 2)
+    assert ey <= TOL[dtype] and es <= TOL[dtype], (ey, es)
