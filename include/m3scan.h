@@ -2,8 +2,9 @@
  * m3scan.h -- C ABI of libm3scan.so, the B300 (sm_103a) Mamba-3 selective
  * SSM scan: a chunked prefill (m3_scan_fwd; m3_scan_fwd_from continues a
  * sequence from a state; m3_scan_fwd_bcnorm fuses the block's B / C
- * normalisation), its backward pass (m3_scan_bwd), a single-token decode
- * step (m3_step) and a k-token decode step (m3_step_k).
+ * normalisation; m3_scan_fwd_host takes host buffers and overlaps the copies
+ * with the scan), its backward pass (m3_scan_bwd), a single-token decode step
+ * (m3_step) and a k-token decode step (m3_step_k).
  *
  * The operation (Mamba-3 summary page, "Mamba-3: Expressive SSM with MIMO"):
  * for every batch row b and head h independently, with scalar A_h < 0 and
@@ -25,8 +26,8 @@
  *
  * Conventions for every entry point:
  *  - Pointers are CUDA device pointers (device memory or managed memory the
- *    device can read) owned by the caller, C-contiguous and aligned to their
- *    element size; the fp32 state / final_state must be 16-byte aligned, and
+ *    device can read; m3_scan_fwd_host's tensors are host memory) owned by
+ *    the caller, C-contiguous and aligned to their element size; the fp32 state / final_state must be 16-byte aligned, and
  *    the tensor-core prefill (M3_ALGO_CHUNKED_TC) also needs x, B, C, theta
  *    and y 16-byte aligned (it returns M3_ERR_ALIGN otherwise).
  *    The library never allocates device memory and never frees a pointer;
@@ -131,6 +132,37 @@ M3_API int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const f
                 const void* B, const void* C, const float* lambda, const void* theta,
                 void* y, float* final_state, void* workspace, size_t workspace_bytes,
                 void* stream);
+
+/* Prefill with inputs and outputs in HOST memory: the scan of m3_scan_fwd for
+ * a caller whose data lives on the host.  The pages have no counterpart; this
+ * is the runtime around the scan: the batch is processed in slices of `slice`
+ * batch rows (every (b, h) sequence is independent, so a slice is a smaller
+ * call of the same kernel and its results are bit-identical to one call over
+ * the whole batch).  Each slice's inputs are copied into one of two device
+ * staging sets in `workspace`, scanned on `stream`, and its y and final_state
+ * copied back; the copies of one slice overlap the scans and copies of the
+ * others (host-to-device and device-to-host run on two streams of the
+ * library's own, forked from and joined back to `stream` with events).
+ *   x, dt, A, B, C, lambda, theta   host memory, layouts and NULL rules as in
+ *                                   m3_scan_fwd (A [h] included)
+ *   y, final_state                  host memory, written (final_state may be NULL)
+ *   Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ *   the copies to overlap; pageable memory works without the overlap.  They
+ *   must stay valid until `stream` completes.
+ *   slice      batch rows per slice, >= 0 (0: ceil(batch / 8); M3_ERR_VALUE if < 0)
+ *   workspace  device memory, 256-byte aligned (M3_ERR_ALIGN), of at least
+ *              m3_scan_fwd_host_workspace_size(d, slice) bytes (M3_ERR_WORKSPACE);
+ *              in use until `stream` completes.
+ * Returns once everything is enqueued; `stream` completes when y and
+ * final_state are in host memory.  The copy streams and their events are made on
+ * a device's first call and kept (handles only: the library still allocates no
+ * device memory); calls from several host threads are serialised while they
+ * enqueue.  T == 0 writes only final_state (zero). */
+M3_API size_t m3_scan_fwd_host_workspace_size(const m3_dims* d, int64_t slice);
+M3_API int m3_scan_fwd_host(const m3_dims* d, const void* x, const float* dt, const float* A,
+                     const void* B, const void* C, const float* lambda, const void* theta,
+                     void* y, float* final_state, int64_t slice, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /* Prefill that continues a sequence: the same computation as m3_scan_fwd,
  * started from a given state instead of zero (the chunked-prefill continuation

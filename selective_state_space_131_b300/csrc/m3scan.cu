@@ -668,6 +668,196 @@ int m3_scan_bwd_noalloc(const m3_dims* d, const void* x, const float* dt, const 
                        has_tokens ? kNoAllocScratchBytes : 0, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// ---- prefill from and to host memory (m3_scan_fwd_host)
+// Per slice of the batch a staging set in the caller's workspace: the inputs
+// x, dt, B, C, lambda, theta and the outputs y, final_state of `slice` batch
+// rows; two sets used in turn, after the heads' A.
+inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct HostSet {
+    size_t x, dt, B, C, lam, th, y, fs, bytes;   // byte offsets inside a set; its size
+};
+
+HostSet host_set(const m3_dims* d, int64_t slice) {
+    const size_t es = d->dtype == M3_F32 ? 4 : 2;
+    const size_t units = (size_t)slice * d->seqlen * d->heads;   // (b, t, h) of one slice
+    HostSet hs;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    hs.x = take(units * d->rank * d->headdim * es);
+    hs.dt = take(units * 4);
+    hs.B = take(units * d->rank * d->dstate * es);
+    hs.C = take(units * d->rank * d->dstate * es);
+    hs.lam = take(units * 4);
+    hs.th = take(units * (d->dstate / 2) * es);
+    hs.y = take(units * d->rank * d->headdim * es);
+    hs.fs = take((size_t)slice * d->heads * d->dstate * d->headdim * 4);
+    hs.bytes = o;
+    return hs;
+}
+
+// batch rows per slice: as asked (at most the batch), or an eighth of the batch
+int64_t host_slice(const m3_dims* d, int64_t slice) {
+    const int64_t b = d->batch > 0 ? d->batch : 1;
+    if (slice > 0) return slice < b ? slice : b;
+    return (b + 7) / 8;
+}
+
+size_t host_ws_bytes(const m3_dims* d, int64_t slice) {
+    return up256((size_t)d->heads * 4) + 2 * host_set(d, slice).bytes;
+}
+
+// The library's two copy streams (host to device, device to host) and its
+// events, per device: made on the device's first call and kept (handles only,
+// no device memory).  A call holds g_pipe_mu while it enqueues, so that calls
+// from several host threads do not interleave their event records.  (Splitting
+// a slice's uploads over two streams measured the same: the host-to-device
+// copies are bound by the link, not by one copy engine.)
+struct HostPipe {
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t fork = nullptr, in[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr},
+                out[2] = {nullptr, nullptr};
+};
+constexpr int kMaxPipeDevices = 256;
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxPipeDevices];
+
+int pipe_for(int dev, HostPipe** out) {
+    HostPipe& p = g_pipe[dev];
+    if (!p.up) {
+        HostPipe q;
+        bool ok = cudaStreamCreateWithFlags(&q.up, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&q.down, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&q.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int k = 0; k < 2 && ok; ++k)
+            ok = cudaEventCreateWithFlags(&q.in[k], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&q.done[k], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&q.out[k], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            cudaEvent_t evs[] = {q.fork, q.in[0], q.in[1], q.done[0], q.done[1], q.out[0], q.out[1]};
+            for (cudaEvent_t e : evs)
+                if (e) cudaEventDestroy(e);
+            if (q.up) cudaStreamDestroy(q.up);
+            if (q.down) cudaStreamDestroy(q.down);
+            return M3_ERR_CUDA;
+        }
+        p = q;
+    }
+    *out = &p;
+    return M3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t m3_scan_fwd_host_workspace_size(const m3_dims* d, int64_t slice) {
+    if (check_dims(d, true) != M3_OK || slice < 0 || d->batch == 0) return 0;
+    return host_ws_bytes(d, host_slice(d, slice));
+}
+
+int m3_scan_fwd_host(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
+                     const float* lambda, const void* theta, void* y, float* final_state, int64_t slice,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_dims(d, true);
+    if (rc != M3_OK) return rc;
+    if (slice < 0) return M3_ERR_VALUE;
+    const bool has_tokens = d->batch > 0 && d->seqlen > 0;
+    if (has_tokens && (!x || !dt || !B || !C || !y)) return M3_ERR_NULL;
+    if (d->batch > 0 && !A) return M3_ERR_NULL;
+    const uintptr_t es = d->dtype == M3_F32 ? 4 : 2;
+    const void* elem_ptrs[] = {x, B, C, theta, y};
+    for (const void* p : elem_ptrs)
+        if (p && !aligned(p, es)) return M3_ERR_ALIGN;
+    const void* f32_ptrs[] = {dt, A, lambda, final_state};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return M3_ERR_ALIGN;
+    if (scan_algorithm(d) == M3_ALGO_NONE) return M3_ERR_UNSUPPORTED;
+    if (d->batch == 0) return M3_OK;
+    const int64_t sl = host_slice(d, slice);
+    if (!workspace || workspace_bytes < host_ws_bytes(d, sl)) return M3_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255) != 0) return M3_ERR_ALIGN;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return M3_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxPipeDevices) return M3_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* p = nullptr;
+    rc = pipe_for(dev, &p);
+    if (rc != M3_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const HostSet hs = host_set(d, sl);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* A_d = reinterpret_cast<float*>(ws);
+    uint8_t* sets = ws + up256((size_t)d->heads * 4);
+    // bytes per batch row of each array
+    const size_t th_units = (size_t)d->seqlen * d->heads;
+    const size_t r_x = th_units * d->rank * d->headdim * es, r_f = th_units * 4;
+    const size_t r_B = th_units * d->rank * d->dstate * es, r_th = th_units * (d->dstate / 2) * es;
+    const size_t r_fs = (size_t)d->heads * d->dstate * d->headdim * 4;
+    const auto up = cudaMemcpyHostToDevice, down = cudaMemcpyDeviceToHost;
+    bool ok = true;
+    auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
+    auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
+
+    // the workspace is free once the caller's earlier work on `stream` is done
+    chk(cudaEventRecord(p->fork, s));
+    chk(cudaStreamWaitEvent(p->up, p->fork, 0));
+    chk(cudaMemcpyAsync(A_d, A, (size_t)d->heads * 4, up, p->up));
+    const int64_t nsl = (d->batch + sl - 1) / sl;
+    int scan_rc = M3_OK;
+    int64_t last = -1;
+    for (int64_t i = 0; i < nsl && ok && scan_rc == M3_OK; ++i) {
+        const int k = (int)(i & 1);
+        const int64_t b0 = i * sl, nb = (d->batch - b0) < sl ? (d->batch - b0) : sl;
+        uint8_t* st = sets + k * hs.bytes;
+        // host -> device, once the set's previous slice has been read back
+        if (i >= 2) chk(cudaStreamWaitEvent(p->up, p->out[k], 0));
+        if (has_tokens) {
+            chk(cudaMemcpyAsync(st + hs.x, at(x, b0 * r_x), nb * r_x, up, p->up));
+            chk(cudaMemcpyAsync(st + hs.dt, at(dt, b0 * r_f), nb * r_f, up, p->up));
+            chk(cudaMemcpyAsync(st + hs.B, at(B, b0 * r_B), nb * r_B, up, p->up));
+            chk(cudaMemcpyAsync(st + hs.C, at(C, b0 * r_B), nb * r_B, up, p->up));
+            if (lambda) chk(cudaMemcpyAsync(st + hs.lam, at(lambda, b0 * r_f), nb * r_f, up, p->up));
+            if (theta) chk(cudaMemcpyAsync(st + hs.th, at(theta, b0 * r_th), nb * r_th, up, p->up));
+        }
+        chk(cudaEventRecord(p->in[k], p->up));
+        // the slice's scan on the caller's stream
+        chk(cudaStreamWaitEvent(s, p->in[k], 0));
+        if (!ok) break;
+        m3_dims ds = *d;
+        ds.batch = nb;
+        scan_rc = m3_scan_fwd(&ds, st + hs.x, reinterpret_cast<const float*>(st + hs.dt), A_d, st + hs.B,
+                              st + hs.C, lambda ? reinterpret_cast<const float*>(st + hs.lam) : nullptr,
+                              theta ? st + hs.th : nullptr, st + hs.y,
+                              final_state ? reinterpret_cast<float*>(st + hs.fs) : nullptr, nullptr, 0, stream);
+        chk(cudaEventRecord(p->done[k], s));
+        // device -> host
+        chk(cudaStreamWaitEvent(p->down, p->done[k], 0));
+        if (has_tokens) chk(cudaMemcpyAsync(static_cast<uint8_t*>(y) + b0 * r_x, st + hs.y, nb * r_x, down, p->down));
+        if (final_state)
+            chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(final_state) + b0 * r_fs, st + hs.fs, nb * r_fs, down,
+                                p->down));
+        chk(cudaEventRecord(p->out[k], p->down));
+        last = i;
+    }
+    // `stream` completes after both copy streams (each in order): the last read-back
+    // and every copy into the workspace
+    if (last >= 0) chk(cudaStreamWaitEvent(s, p->out[last & 1], 0));
+    chk(cudaEventRecord(p->fork, p->up));
+    chk(cudaStreamWaitEvent(s, p->fork, 0));
+    if (scan_rc != M3_OK) return scan_rc;
+    return ok ? M3_OK : M3_ERR_CUDA;
+}
+
 int m3_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return M3_ERR_CUDA;
     unsigned int v = 0;

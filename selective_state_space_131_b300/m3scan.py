@@ -46,6 +46,10 @@ _lib.m3_scan_fwd_from.argtypes = [_dp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_fwd_from.restype = ctypes.c_int
 _lib.m3_scan_fwd_bcnorm.argtypes = [_dp] + [_vp] * 11 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_size_t, _vp]
 _lib.m3_scan_fwd_bcnorm.restype = ctypes.c_int
+_lib.m3_scan_fwd_host_workspace_size.argtypes = [_dp, ctypes.c_int64]
+_lib.m3_scan_fwd_host_workspace_size.restype = ctypes.c_size_t
+_lib.m3_scan_fwd_host.argtypes = [_dp] + [_vp] * 9 + [ctypes.c_int64, _vp, ctypes.c_size_t, _vp]
+_lib.m3_scan_fwd_host.restype = ctypes.c_int
 _lib.m3_step.argtypes = [_dp] + [_vp] * 11 + [_vp]
 _lib.m3_step.restype = ctypes.c_int
 _lib.m3_scan_bwd_workspace_size.argtypes = [_dp]
@@ -140,6 +144,26 @@ def m3_scan_fwd(x, dt, A, B, C, lam, theta, y, final_state, chunk: int = 64, wor
                           _stream(stream))
     if rc != M3_OK:
         raise M3Error(rc, "m3_scan_fwd")
+
+
+def m3_scan_fwd_host_workspace_size(dims: m3_dims, slice: int = 0) -> int:
+    """Device workspace bytes of m3_scan_fwd_host for these sizes and slice."""
+    return int(_lib.m3_scan_fwd_host_workspace_size(ctypes.byref(dims), int(slice)))
+
+
+def m3_scan_fwd_host(x, dt, A, B, C, lam, theta, y, final_state, workspace, workspace_bytes: int, slice: int = 0,
+                     chunk: int = 64, stream=None, dims: m3_dims | None = None) -> None:
+    """Prefill with every tensor in host memory (CPU tensors, page-locked for the
+    copies to overlap), the batch in slices of `slice` rows staged through the
+    device `workspace`; y / final_state are complete once `stream` is.  Raises
+    M3Error."""
+    if dims is None:
+        dims = scan_dims(x, B, chunk)
+    rc = _lib.m3_scan_fwd_host(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(lam),
+                               _ptr(theta), _ptr(y), _ptr(final_state), int(slice), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream))
+    if rc != M3_OK:
+        raise M3Error(rc, "m3_scan_fwd_host")
 
 
 def m3_scan_fwd_from(x, dt, A, B, C, lam, theta, initial_state, prev_B, prev_x, y, final_state, chunk: int = 64,
@@ -268,6 +292,13 @@ def raw_scan_fwd(dims: m3_dims, ptrs, stream=None) -> int:
     workspace, workspace_bytes); returns the status code."""
     *p, ws_bytes = ptrs
     return int(_lib.m3_scan_fwd(ctypes.byref(dims), *p, int(ws_bytes), stream))
+
+
+def raw_scan_fwd_host(dims: m3_dims, ptrs, slice: int = 0, stream=None) -> int:
+    """Direct call with raw addresses (x, dt, A, B, C, lam, theta, y, final_state,
+    workspace, workspace_bytes) and the slice; returns the status code."""
+    *p, ws, ws_bytes = ptrs
+    return int(_lib.m3_scan_fwd_host(ctypes.byref(dims), *p, int(slice), ws, int(ws_bytes), stream))
 
 
 def raw_scan_fwd_from(dims: m3_dims, ptrs, stream=None) -> int:

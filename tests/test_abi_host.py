@@ -219,3 +219,28 @@ def test_bwd_validation(m3):
     assert m3.raw_scan_bwd(_dims(m3, rank=2, chunk=64), _bwd_ptrs()) == m3.M3_ERR_UNSUPPORTED
     assert m3.m3_scan_bwd_workspace_size(_dims(m3, chunk=128)) == 0
     assert m3.raw_scan_bwd(_dims(m3, dstate=7), _bwd_ptrs()) == m3.M3_ERR_SHAPE
+
+
+def test_scan_fwd_host_validation(m3):
+    """The host-buffer prefill: its workspace size and the arguments it rejects
+    before touching a stream (no GPU here)."""
+    d = _dims(m3)    # b2 T100 h4 P64 N64 R1 bf16
+    per_row = 100 * 4 * (64 * 2 * 2 + 4 + 64 * 2 * 2 + 4 + 32 * 2)   # x, dt, B, C, lambda, theta, y of one row
+    one = m3.m3_scan_fwd_host_workspace_size(d, 1)
+    two = m3.m3_scan_fwd_host_workspace_size(d, 2)
+    assert one >= 2 * (per_row + 4 * 64 * 64 * 4) and 1.9 * one < two < 2 * one
+    assert m3.m3_scan_fwd_host_workspace_size(d, 0) == one            # default: ceil(2 / 8) = 1 row
+    assert m3.m3_scan_fwd_host_workspace_size(d, 50) == two           # at most the batch
+    assert m3.m3_scan_fwd_host_workspace_size(d, -1) == 0
+    assert m3.m3_scan_fwd_host_workspace_size(_dims(m3, batch=0), 1) == 0
+    assert m3.m3_scan_fwd_host_workspace_size(_dims(m3, dstate=63), 1) == 0
+    ok = dict(ws=FAKE, wsb=one)
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(**ok), slice=-1) == m3.M3_ERR_VALUE
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(x=None, **ok)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(A=None, **ok)) == m3.M3_ERR_NULL
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(y=FAKE + 1, **ok)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(ws=FAKE, wsb=one - 1)) == m3.M3_ERR_WORKSPACE
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(ws=None, wsb=one)) == m3.M3_ERR_WORKSPACE
+    assert m3.raw_scan_fwd_host(d, _scan_ptrs(ws=FAKE + 16, wsb=one)) == m3.M3_ERR_ALIGN
+    assert m3.raw_scan_fwd_host(_dims(m3, dstate=63), _scan_ptrs(**ok)) == m3.M3_ERR_SHAPE
+    assert m3.raw_scan_fwd_host(_dims(m3, batch=0), _scan_ptrs(x=None, y=None, ws=None, wsb=0)) == m3.M3_OK
