@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "step_simt.cuh"
 #include "step_fast.cuh"
+#include "step_k.cuh"
 #include "step_ring.cuh"
 #include "scan_ws.cuh"
 #include "scan_chunk.cuh"
