@@ -45,9 +45,9 @@ NCU_TRAFFIC = {
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
                                       "sha256": "dc6d5e6015abf56b"},
     # decode: one step of the 1024-step sweep (graph replay), per launch
-    "decode_f32_b256h32P64N64_R1": {"bytes": 145.835264e6 + 77.099520e6,
+    "decode_f32_b256h32P64N64_R1": {"bytes": 145.839360e6 + 76.878080e6,
                                     "source": "selective_state_space_131_b300/csrc/step_fast.cuh",
-                                    "sha256": "dcdb0919045c3efd"},
+                                    "sha256": "c66af4ad5288320a"},
     "decode_f32_b256h32P64N64_R4": {"bytes": 177.312768e6 + 84.965120e6,
                                     "source": "selective_state_space_131_b300/csrc/step_ring.cuh",
                                     "sha256": "8cd37f266fbcedb5"},
