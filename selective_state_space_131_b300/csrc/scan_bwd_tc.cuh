@@ -218,34 +218,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 8; ++q) ptx::cp_async16(dst + 4 * q, src + 4 * q);
         ptx::cp_async_commit();
     };
-    // warps 6 and 7: dtheta of chunk cc from its rows' dPhi (F_DPR), suffix sums in
-    // two segments of Q / 2 tokens per pair, carried from the chunks after it
+    // warpgroup 0 (idle while warpgroup 1 runs the mask's column sums and the token
+    // scalars): dtheta of chunk cc from its rows' dPhi (F_DPR), suffix sums over the
+    // 64 rows in four segments of 16 (warp = segment, lane = pair), carried from the
+    // chunks after it; the sum at a token's first row is that token's dtheta
     auto dtheta_chunk = [&](int cc) {
-        const int seg = warp - 6;
-        constexpr int QS = Q / 2;
+        const int seg = warp;
+        constexpr int RS = 16;
         const int64_t tc0 = (int64_t)cc * Q;
         const int ntc = (int)((T - tc0) < Q ? (T - tc0) : Q);
-        float v[QS];
+        float v[RS];
         float tot = 0.0f;
 #pragma unroll
-        for (int q = 0; q < QS; ++q) {
-            const int t = seg * QS + q;
-            float a = 0.0f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) a += F[F_DPR + (t * R + r) * KS + lane];
-            v[q] = a;
-            tot += a;
+        for (int q = 0; q < RS; ++q) {
+            v[q] = F[F_DPR + (seg * RS + q) * KS + lane];
+            tot += v[q];
         }
         F[F_SEG + seg * 32 + lane] = tot;
-        ptx::bar_sync(3, 64);
-        float acc = F[F_DPHI + lane] + (seg == 0 ? F[F_SEG + 32 + lane] : 0.0f);
+        ptx::bar_sync(3, 128);
+        float acc = F[F_DPHI + lane];
+        for (int s2 = seg + 1; s2 < 4; ++s2) acc += F[F_SEG + s2 * 32 + lane];
 #pragma unroll
-        for (int q = QS - 1; q >= 0; --q) {
-            const int t = seg * QS + q;
+        for (int q = RS - 1; q >= 0; --q) {
+            const int rw = seg * RS + q;
             acc += v[q];
-            if (t < ntc) prm.dtheta[(((int64_t)b * T + tc0 + t) * prm.H + h) * K + lane] = __float2bfloat16_rn(acc);
+            if (rw % R == 0 && rw / R < ntc)
+                prm.dtheta[(((int64_t)b * T + tc0 + rw / R) * prm.H + h) * K + lane] = __float2bfloat16_rn(acc);
         }
-        ptx::bar_sync(3, 64);
+        ptx::bar_sync(3, 128);   // every thread has read F_DPHI
         if (seg == 0) F[F_DPHI + lane] = acc;
     };
     auto issue_scalars = [&](int c, int st) {
@@ -629,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::umma_commit(&bar_m2);
         }
         __syncwarp();
+        if (wg == 0 && prm.theta && c + 1 < nch) dtheta_chunk(c + 1);
         if (wg == 1) {
             // column sums of dM o M (threads 128-191) and dM o E (192-255)
             const int j = (tid - 128) & 63;
@@ -641,7 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             F[(tid < 192 ? F_CZM : F_CZE) + j] = a0 + a1;
             ptx::bar_sync(2, 128);
-            if (warp >= 6 && prm.theta && c + 1 < nch) dtheta_chunk(c + 1);
             if (warp == 6 && prm.theta && c == nch - 1) {
                 // the final state's angle term: the part through G_{nch-1}, decayed over
                 // the chunk, and the part through the chunk's rows but the last token's
@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dA_acc += dA_c;
             }
         }
-        if (wg == 1) ptx::bar_sync(2, 128);   // dtheta has read F_DPR before epilogue 2 rewrites it
+        ptx::bar_sync(4, kThreads);   // warpgroup 0's dtheta has read F_DPR before epilogue 2 rewrites it
         if (!ptx::mbar_wait(&bar_m2, (nch - 1 - c) & 1, kWaitBudget)) {
             m3::set_status(m3::kStatusWaitTimeout);
             abort_s = 1;
@@ -876,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     }
     // dtheta of chunk 0 (the last chunk processed)
-    if (!fail && warp >= 6 && prm.theta) dtheta_chunk(0);
+    if (!fail && wg == 0 && prm.theta) dtheta_chunk(0);
     if (tid == 128) prm.dA_part[unit] = dA_acc;   // warp 4 lane 0 accumulated it
     if (fail && tid == 32) {
         // stopped early: wait (bounded) for the last load of each stage
