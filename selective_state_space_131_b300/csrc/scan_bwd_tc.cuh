@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int K = 32;          // rotation pairs (N = 64)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_ld[2], bar_m1, bar_m2, bar_fin;
+    __shared__ uint64_t bar_ld[2], bar_ck[2], bar_m1, bar_m2, bar_fin;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_s;
     if (blockDim.x != kThreads) {
@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         ptx::mbar_init(&bar_ld[0], 1);
         ptx::mbar_init(&bar_ld[1], 1);
+        ptx::mbar_init(&bar_ck[0], 1);
+        ptx::mbar_init(&bar_ck[1], 1);
         ptx::mbar_init(&bar_m1, 1);
         ptx::mbar_init(&bar_m2, 1);
         ptx::mbar_init(&bar_fin, 1);
@@ -209,14 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_5d(base + ST_DY, &map_dy, &bar_ld[st], 0, 0, h, t0, b);
         if (rot) ptx::tma_load_4d(base + ST_TH, &map_th, &bar_ld[st], 0, h, t0, b);
     };
-    // warpgroup 0: each thread copies its own slice (row `row`, columns 32 hc ..) of
-    // checkpoint slot c into stage st of the fp32 buffer (it alone reads it back)
+    // thread 0: checkpoint slot c (the fp32 64 x 64 state, 16 KB, contiguous) into
+    // stage st of the fp32 buffer with one bulk copy (one instruction instead of a
+    // 16-byte copy per thread and vector)
+    int ck_count[2] = {0, 0};   // thread 0: copies issued per stage
     auto issue_ckpt = [&](int c, int st) {
-        const float* src = prm.ck_G + (((int64_t)unit * (prm.nch + 1) + c) * 64 + row) * 64 + 32 * hc;
-        float* dst = reinterpret_cast<float*>(smem + OFF_GB) + st * 4096 + row * 64 + 32 * hc;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ptx::cp_async16(dst + 4 * q, src + 4 * q);
-        ptx::cp_async_commit();
+        ++ck_count[st];
+        ptx::mbar_arrive_expect_tx(&bar_ck[st], 64 * 64 * 4);
+        ptx::bulk_g2s(smem + OFF_GB + st * 16384, prm.ck_G + ((int64_t)unit * (prm.nch + 1) + c) * 64 * 64,
+                      64 * 64 * 4, &bar_ck[st]);
     };
     // warpgroup 0 (idle while warpgroup 1 runs the mask's column sums and the token
     // scalars): dtheta of chunk cc from its rows' dPhi (F_DPR), suffix sums over the
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
     if (tid == 32) issue_loads(nch - 1, (nch - 1) & 1);
     if (warp == 7) issue_scalars(nch - 1, (nch - 1) & 1);
-    if (wg == 0) issue_ckpt(nch - 1, (nch - 1) & 1);
+    if (tid == 0) issue_ckpt(nch - 1, (nch - 1) & 1);
     bool fail = false;
     float dA_acc = 0.0f;
 
@@ -313,10 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next chunk (in reverse) into the other stage, free since the
         // previous iteration's batch 2 completed
         if (c > 0 && tid == 32) issue_loads(c - 1, st ^ 1);
+        if (c > 0 && tid == 0) issue_ckpt(c - 1, st ^ 1);   // its stage was read last iteration
         // ---- (1) checkpoint G_{c-1} (warpgroup 0: fp32 slice for <dG, G>, bf16 tile;
         //      the next chunk's slice prefetched); dt / lambda (warp 7)
         if (wg == 0) {
-            ptx::cp_async_wait_all();   // this thread's slice of slot c
+            // slot c (copied during the chunk before)
+            if (!ptx::mbar_wait(&bar_ck[st], ((nch - 1 - c) >> 1) & 1, kWaitBudget)) {
+                m3::set_status(m3::kStatusWaitTimeout);
+                abort_s = 1;
+            }
             float gsl[32];
             const float* src = reinterpret_cast<const float*>(smem + OFF_GB) + st * 4096 + row * 64 + 32 * hc;
 #pragma unroll
@@ -324,7 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4 v = *reinterpret_cast<const float4*>(src + 4 * p4);
                 gsl[4 * p4] = v.x; gsl[4 * p4 + 1] = v.y; gsl[4 * p4 + 2] = v.z; gsl[4 * p4 + 3] = v.w;
             }
-            if (c > 0) issue_ckpt(c - 1, st ^ 1);
             tile_put32(smem + OFF_G, row, hc, gsl);
             float part = 0.0f;
 #pragma unroll
@@ -878,6 +885,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dtheta of chunk 0 (the last chunk processed)
     if (!fail && wg == 0 && prm.theta) dtheta_chunk(0);
     if (tid == 128) prm.dA_part[unit] = dA_acc;   // warp 4 lane 0 accumulated it
+    if (fail && tid == 0) {
+        // stopped early: the checkpoint copies in flight land (bounded wait)
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (ck_count[s2] > 0) (void)ptx::mbar_wait(&bar_ck[s2], (ck_count[s2] - 1) & 1, kWaitBudget);
+    }
     if (fail && tid == 32) {
         // stopped early: wait (bounded) for the last load of each stage
         for (int s2 = 0; s2 < 2; ++s2)
