@@ -156,8 +156,8 @@ M3_API int m3_scan_fwd(const m3_dims* d, const void* x, const float* dt, const f
  * Returns once everything is enqueued; `stream` completes when y and
  * final_state are in host memory.  The copy streams and their events are made on
  * a device's first call and kept (handles only: the library still allocates no
- * device memory); calls from several host threads are serialised while they
- * enqueue.  T == 0 writes only final_state (zero). */
+ * device memory; made again after a device reset); calls from several host
+ * threads are serialised while they enqueue.  T == 0 writes only final_state (zero). */
 M3_API size_t m3_scan_fwd_host_workspace_size(const m3_dims* d, int64_t slice);
 M3_API int m3_scan_fwd_host(const m3_dims* d, const void* x, const float* dt, const float* A,
                      const void* B, const void* C, const float* lambda, const void* theta,
@@ -269,8 +269,8 @@ M3_API int m3_scan_bwd(const m3_dims* d, const void* x, const float* dt, const f
  *   - Sizes whose workspace (m3_scan_bwd_workspace_size) exceeds 32 MiB are
  *     rejected with M3_ERR_WORKSPACE before anything runs.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and keeps it; make that first call before any
- *     stream capture.
+ *     that device current) and keeps it, per context (after a device reset
+ *     it is looked up again); make that first call before any stream capture.
  *   - Every call on a device shares the one array.  Calls whose work overlaps
  *     on the GPU (other streams, other host threads) race on it and corrupt
  *     each other's result: order them on one stream or synchronise.  No part of

@@ -625,22 +625,47 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 static __device__ __align__(256) uint8_t g_bwd_scratch[kNoAllocScratchBytes];
 
-// The device address of g_bwd_scratch, looked up once per device with that
-// device current (in host code the array's name is a host-side stand-in, not a
-// device address).
+// The context current on the calling thread (driver API, looked up once through
+// the runtime): the per-device caches below are keyed by it, so that a device
+// reset (a new primary context, where the old addresses and handles are void)
+// makes them look up again instead of using stale ones.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+int current_context(CUcontext* out) {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return M3_ERR_CUDA;
+        fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    if (fn(out) == CUDA_SUCCESS && *out) return M3_OK;
+    // no context current on this thread yet: the runtime makes the device's primary one
+    if (cudaFree(nullptr) != cudaSuccess) return M3_ERR_CUDA;
+    return fn(out) == CUDA_SUCCESS && *out ? M3_OK : M3_ERR_CUDA;
+}
+
+// The device address of g_bwd_scratch, looked up once per device and context
+// with that device current (in host code the array's name is a host-side
+// stand-in, not a device address).
 constexpr int kMaxScratchDevices = 256;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxScratchDevices];
+CUcontext g_scratch_ctx[kMaxScratchDevices];
 
 int scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return M3_ERR_CUDA;
     if (dev < 0 || dev >= kMaxScratchDevices) return M3_ERR_UNSUPPORTED;
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != M3_OK) return M3_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return M3_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return M3_OK;
@@ -723,6 +748,7 @@ size_t host_ws_bytes(const m3_dims* d, int64_t slice) {
 // a slice's uploads over two streams measured the same: the host-to-device
 // copies are bound by the link, not by one copy engine.)
 struct HostPipe {
+    CUcontext ctx = nullptr;   // the context the handles belong to
     cudaStream_t up = nullptr, down = nullptr;
     cudaEvent_t fork = nullptr, in[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr},
                 out[2] = {nullptr, nullptr};
@@ -733,8 +759,13 @@ HostPipe g_pipe[kMaxPipeDevices];
 
 int pipe_for(int dev, HostPipe** out) {
     HostPipe& p = g_pipe[dev];
-    if (!p.up) {
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != M3_OK) return M3_ERR_CUDA;
+    // handles made in an earlier context (before a device reset) are void: made again
+    // (the old ones went with their context)
+    if (!p.up || p.ctx != ctx) {
         HostPipe q;
+        q.ctx = ctx;
         bool ok = cudaStreamCreateWithFlags(&q.up, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&q.down, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&q.fork, cudaEventDisableTiming) == cudaSuccess;

@@ -109,3 +109,4 @@ def test_host_prefill_empty_sequence_writes_zero_state(m3):
                         dims=dims)
     torch.cuda.synchronize()
     assert torch.count_nonzero(fs) == 0
+
