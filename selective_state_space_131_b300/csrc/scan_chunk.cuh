@@ -238,47 +238,128 @@ __global__ void __launch_bounds__(kThreads) m3_scan_chunk_kernel(
             __syncthreads();
         }
 
-        // ---- (4) y, one block of RB rows at a time
+        // ---- (4) y, one block of RB rows at a time.  Every thread computes 4 x 4 tiles
+        //      (four rows by four columns), so that each value read from shared memory
+        //      feeds four multiply-adds.
         for (int rb0 = 0; rb0 < QR; rb0 += geo.RB) {
-            const int rows = (QR - rb0) < geo.RB ? (QR - rb0) : geo.RB;
+            const int rows = (QR - rb0) < geo.RB ? (QR - rb0) : geo.RB;   // a multiple of 16
             const int jmax = ((rb0 + rows - 1) / R + 1) * R;   // columns up to the block's last token
-            for (int e = tid; e < rows * jmax; e += kThreads) {
-                const int il = e / jmax, j = e % jmax, i = rb0 + il;
-                const int ti = i / R, tj = j / R;
-                float v = 0.0f;
-                if (tj <= ti) {
-                    float dot = 0.0f;
-                    for (int n = 0; n < N; ++n) dot = fmaf(Stage<T>::get(Ct, i * NS + n), Stage<T>::get(Bt, j * NS + n), dot);
-                    const float mk = (tj == ti) ? sc_gam[ti] : expf(sc_cs[ti] - sc_cs[tj]) * sc_w[tj];
-                    v = dot * mk;
+            const int jt = (jmax + 3) / 4;                      // 4-column tiles (<= QR / 4)
+            // (4a) S' = (C~ B~^T) o M for rows [rb0, rb0 + rows), columns [0, 4 jt)
+            for (int tt = tid; tt < (rows / 4) * jt; tt += kThreads) {
+                const int il0 = (tt / jt) * 4, j0 = (tt % jt) * 4;
+                const int i0 = rb0 + il0;
+                float acc[4][4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[a][q] = 0.0f;
+                if (j0 / R <= (i0 + 3) / R) {   // some entry on or below the diagonal
+                    for (int n = 0; n < N; ++n) {
+                        float cv[4], bv[4];
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) cv[a] = Stage<T>::get(Ct, (i0 + a) * NS + n);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) bv[q] = Stage<T>::get(Bt, (j0 + q) * NS + n);
+#pragma unroll
+                        for (int a = 0; a < 4; ++a)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(cv[a], bv[q], acc[a][q]);
+                    }
                 }
-                Sp[il * QR + j] = v;
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const int ti = (i0 + a) / R;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = j0 + q, tj = j / R;
+                        float v = 0.0f;
+                        if (tj <= ti) {
+                            const float mk = (tj == ti) ? sc_gam[ti] : expf(sc_cs[ti] - sc_cs[tj]) * sc_w[tj];
+                            v = acc[a][q] * mk;
+                        }
+                        Sp[(il0 + a) * QR + j] = v;
+                    }
+                }
             }
             __syncthreads();
-            for (int e = tid; e < rows * P; e += kThreads) {
-                const int il = e / P, p = e % P, i = rb0 + il;
-                const int ti = i / R;
-                if (ti >= nt) continue;
-                const int jn = (ti + 1) * R;
-                float acc = 0.0f;
-                for (int j = 0; j < jn; ++j) acc = fmaf(Sp[il * QR + j], Stage<T>::get(Xs, j * P + p), acc);
-                float inter = 0.0f;
-                for (int n = 0; n < N; ++n) inter = fmaf(Stage<T>::get(Ct, i * NS + n), G[n * P + p], inter);
-                acc = fmaf(sc_ecs[ti], inter, acc);
-                m3::IO<T>::st(y, tok_idx(t0 + ti) * R * P + (i - ti * R) * P + p, acc);
+            // (4b) y = S' X + diag(exp cs) C~ G_{c-1} for the block's rows, 4 x 4 tiles of (row, p)
+            const int pt = P / 4;
+            for (int tt = tid; tt < (rows / 4) * pt; tt += kThreads) {
+                const int il0 = (tt / pt) * 4, p0 = (tt % pt) * 4;
+                const int i0 = rb0 + il0;
+                const int jn = ((i0 + 3) / R + 1) * R;   // columns up to the last row's token
+                float acc[4][4], inter[4][4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) { acc[a][q] = 0.0f; inter[a][q] = 0.0f; }
+                for (int j = 0; j < jn; ++j) {
+                    float sv[4], xv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) sv[a] = Sp[(il0 + a) * QR + j];   // zero past each row's token
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xv[q] = Stage<T>::get(Xs, j * P + p0 + q);
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(sv[a], xv[q], acc[a][q]);
+                }
+                for (int n = 0; n < N; ++n) {
+                    float cv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) cv[a] = Stage<T>::get(Ct, (i0 + a) * NS + n);
+                    const float4 g4 = *reinterpret_cast<const float4*>(G + n * P + p0);
+                    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) inter[a][q] = fmaf(cv[a], gv[q], inter[a][q]);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const int i = i0 + a, ti = i / R;
+                    if (ti >= nt) continue;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        m3::IO<T>::st(y, tok_idx(t0 + ti) * R * P + (i - ti * R) * P + p0 + q,
+                                      fmaf(sc_ecs[ti], inter[a][q], acc[a][q]));
+                }
             }
             __syncthreads();
         }
 
-        // ---- (5) G_c = exp(cs_end) G_{c-1} + sum_j dec_tj B~_j x_j^T
+        // ---- (5) G_c = exp(cs_end) G_{c-1} + sum_j dec_tj B~_j x_j^T, 4 x 4 tiles of (n, p)
         {
             const float dec_end = expf(sc_cs[Q - 1]);
-            for (int e = tid; e < N * P; e += kThreads) {
-                const int n = e / P, p = e % P;
-                float acc = 0.0f;
-                for (int j = 0; j < QR; ++j)
-                    acc = fmaf(sc_dec[j / R] * Stage<T>::get(Bt, j * NS + n), Stage<T>::get(Xs, j * P + p), acc);
-                G[e] = fmaf(dec_end, G[e], acc);
+            const int nt4 = (N + 3) / 4, pt = P / 4;
+            for (int tt = tid; tt < nt4 * pt; tt += kThreads) {
+                const int n0 = (tt / pt) * 4, p0 = (tt % pt) * 4;
+                float acc[4][4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[a][q] = 0.0f;
+                for (int j = 0; j < QR; ++j) {
+                    const float dj = sc_dec[j / R];
+                    float bv[4], xv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) bv[a] = (n0 + a < N) ? dj * Stage<T>::get(Bt, j * NS + n0 + a) : 0.0f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xv[q] = Stage<T>::get(Xs, j * P + p0 + q);
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(bv[a], xv[q], acc[a][q]);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    if (n0 + a >= N) break;
+                    float4* gp = reinterpret_cast<float4*>(G + (n0 + a) * P + p0);
+                    const float4 g = *gp;
+                    *gp = make_float4(fmaf(dec_end, g.x, acc[a][0]), fmaf(dec_end, g.y, acc[a][1]),
+                                      fmaf(dec_end, g.z, acc[a][2]), fmaf(dec_end, g.w, acc[a][3]));
+                }
             }
         }
         __syncthreads();
