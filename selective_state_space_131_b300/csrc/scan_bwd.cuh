@@ -248,11 +248,28 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_ckpt_kernel(const Geo geo, Wo
             __syncthreads();
         }
         const float dec_end = expf(cs[Q - 1]);
-        for (int e = tid; e < N * P; e += kThreads) {
-            const int n = e / P, p = e % P;
-            float acc = 0.0f;
-            for (int j = 0; j < QR; ++j) acc = fmaf(sdec[j / R] * Bt[j * NS + n], Xs[j * PS + p], acc);
-            G[e] = fmaf(dec_end, G[e], acc);
+        // 4 x 4 tiles of (n, p): each value read from shared memory feeds four products
+        for (int tt = tid; tt < ((N + 3) / 4) * (P / 4); tt += kThreads) {
+            const int n0 = (tt / (P / 4)) * 4, p0 = (tt % (P / 4)) * 4;
+            float acc[4][4] = {};
+            for (int j = 0; j < QR; ++j) {
+                const float dj = sdec[j / R];
+                float bv[4], xv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) bv[a] = (n0 + a < N) ? dj * Bt[j * NS + n0 + a] : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) xv[q] = Xs[j * PS + p0 + q];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(bv[a], xv[q], acc[a][q]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (n0 + a >= N) break;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) G[(n0 + a) * P + p0 + q] = fmaf(dec_end, G[(n0 + a) * P + p0 + q], acc[a][q]);
+            }
         }
         __syncthreads();
     }
@@ -417,31 +434,78 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
             __syncthreads();
         }
         // ---- (3) S' = S o M, dS = dS' o M, dM = dS' o S;  T2 = dY G^T;  XG = X dG^T
-        for (int e = tid; e < QR * QR; e += kThreads) {
-            const int i = e / QR, j = e % QR, ti = i / R, tj = j / R;
-            float sp = 0.0f, dsv = 0.0f, z = 0.0f;
-            if (tj <= ti) {
-                float s = 0.0f, dsp = 0.0f;
-                for (int n = 0; n < N; ++n) s = fmaf(Ct[i * NS + n], Bt[j * NS + n], s);
-                for (int p = 0; p < P; ++p) dsp = fmaf(dYs[i * PS + p], Xs[j * PS + p], dsp);
-                const float m = (tj == ti) ? gam[ti] : expf(cs[ti] - cs[tj]) * wv[tj];
-                sp = s * m;
-                dsv = dsp * m;
-                z = dsp * s;
+        //      (4 x 4 tiles: each value read from shared memory feeds four products; the
+        //      sums keep their order)
+        for (int tt = tid; tt < (QR / 4) * (QR / 4); tt += kThreads) {
+            const int i0 = (tt / (QR / 4)) * 4, j0 = (tt % (QR / 4)) * 4;
+            float sa[4][4] = {}, da[4][4] = {};
+            if (j0 / R <= (i0 + 3) / R) {   // some entry on or below the diagonal
+                for (int n = 0; n < N; ++n) {
+                    float cv[4], bv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) { cv[a] = Ct[(i0 + a) * NS + n]; bv[a] = Bt[(j0 + a) * NS + n]; }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) sa[a][q] = fmaf(cv[a], bv[q], sa[a][q]);
+                }
+                for (int p = 0; p < P; ++p) {
+                    float yv[4], xv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) { yv[a] = dYs[(i0 + a) * PS + p]; xv[a] = Xs[(j0 + a) * PS + p]; }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) da[a][q] = fmaf(yv[a], xv[q], da[a][q]);
+                }
             }
-            Sp[i * QS + j] = sp;
-            dS[i * QS + j] = dsv;
-            Zm[i * QS + j] = z;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int i = i0 + a, ti = i / R;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = j0 + q, tj = j / R;
+                    float sp = 0.0f, dsv = 0.0f, z = 0.0f;
+                    if (tj <= ti) {
+                        const float m = (tj == ti) ? gam[ti] : expf(cs[ti] - cs[tj]) * wv[tj];
+                        sp = sa[a][q] * m;
+                        dsv = da[a][q] * m;
+                        z = da[a][q] * sa[a][q];
+                    }
+                    Sp[i * QS + j] = sp;
+                    dS[i * QS + j] = dsv;
+                    Zm[i * QS + j] = z;
+                }
+            }
         }
-        for (int e = tid; e < QR * N; e += kThreads) {
-            const int i = e / N, n = e % N;
-            float a2 = 0.0f, ax = 0.0f;
+        for (int tt = tid; tt < (QR / 4) * ((N + 3) / 4); tt += kThreads) {
+            const int i0 = (tt / ((N + 3) / 4)) * 4, n0 = (tt % ((N + 3) / 4)) * 4;
+            float a2[4][4] = {}, ax[4][4] = {};
             for (int p = 0; p < P; ++p) {
-                a2 = fmaf(dYs[i * PS + p], G[n * PS + p], a2);
-                ax = fmaf(Xs[i * PS + p], dG[n * PS + p], ax);
+                float yv[4], xv[4], gv[4], dv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    yv[a] = dYs[(i0 + a) * PS + p];
+                    xv[a] = Xs[(i0 + a) * PS + p];
+                    gv[a] = (n0 + a < N) ? G[(n0 + a) * PS + p] : 0.0f;
+                    dv[a] = (n0 + a < N) ? dG[(n0 + a) * PS + p] : 0.0f;
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        a2[a][q] = fmaf(yv[a], gv[q], a2[a][q]);
+                        ax[a][q] = fmaf(xv[a], dv[q], ax[a][q]);
+                    }
             }
-            T2[i * NS + n] = a2;
-            XG[i * NS + n] = ax;
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (n0 + q < N) {
+                        T2[(i0 + a) * NS + n0 + q] = a2[a][q];
+                        XG[(i0 + a) * NS + n0 + q] = ax[a][q];
+                    }
         }
         // <dG_c, G_{c-1}>: the gradient of exp(cs_end) through the state
         {
@@ -469,14 +533,36 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
         __syncthreads();
         // ---- (5) dX, dC~ (into T2), dB~ (into XG) -- each thread reads only the
         //      T2 / XG element it overwrites
-        for (int e = tid; e < QR * P; e += kThreads) {
-            const int j = e / P, p = e % P, tj = j / R;
-            float acc = 0.0f;
-            for (int i = tj * R; i < QR; ++i) acc = fmaf(Sp[i * QS + j], dYs[i * PS + p], acc);
-            float st = 0.0f;
-            for (int n = 0; n < N; ++n) st = fmaf(Bt[j * NS + n], dG[n * PS + p], st);
-            acc = fmaf(sv[tj], st, acc);
-            if (tj < nt) m3::IO<T>::st(dx, tok_idx(t0 + tj) * R * P + (j - tj * R) * P + p, acc);
+        for (int tt = tid; tt < (QR / 4) * (P / 4); tt += kThreads) {
+            const int j0 = (tt / (P / 4)) * 4, p0 = (tt % (P / 4)) * 4;
+            float acc[4][4] = {}, st[4][4] = {};
+            // rows from the first column's token on (S' is zero above each column's token)
+            for (int i = (j0 / R) * R; i < QR; ++i) {
+                float sv4[4], yv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) { sv4[a] = Sp[i * QS + j0 + a]; yv[a] = dYs[i * PS + p0 + a]; }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(sv4[a], yv[q], acc[a][q]);
+            }
+            for (int n = 0; n < N; ++n) {
+                float bv[4], gv[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) { bv[a] = Bt[(j0 + a) * NS + n]; gv[a] = dG[n * PS + p0 + a]; }
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st[a][q] = fmaf(bv[a], gv[q], st[a][q]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int j = j0 + a, tj = j / R;
+                if (tj >= nt) continue;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    m3::IO<T>::st(dx, tok_idx(t0 + tj) * R * P + (j - tj * R) * P + p0 + q, fmaf(sv[tj], st[a][q], acc[a][q]));
+            }
         }
         // dC~_i = sum_j dS_ij B~_j + exp(cs_i) T2_i and dB~_j = sum_i dS_ij C~_i + s_j XG_j,
         // one thread per row and rotation pair.  The same-token block's share (j, i in
@@ -659,11 +745,29 @@ __global__ void __launch_bounds__(kThreads) m3_bwd_chunk_kernel(
         // ---- (8) dG_{c-1} = exp(cs_end) dG_c + C~^T diag(exp(cs)) dY  (C~ still rotated)
         {
             const float dec_end = expf(cs[Q - 1]);
-            for (int e = tid; e < N * P; e += kThreads) {
-                const int n = e / P, p = e % P;
-                float acc = 0.0f;
-                for (int i = 0; i < QR; ++i) acc = fmaf(Ct[i * NS + n] * ecs[i / R], dYs[i * PS + p], acc);
-                dG[n * PS + p] = fmaf(dec_end, dG[n * PS + p], acc);
+            for (int tt = tid; tt < ((N + 3) / 4) * (P / 4); tt += kThreads) {
+                const int n0 = (tt / (P / 4)) * 4, p0 = (tt % (P / 4)) * 4;
+                float acc[4][4] = {};
+                for (int i = 0; i < QR; ++i) {
+                    const float ei = ecs[i / R];
+                    float cv[4], yv[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        cv[a] = (n0 + a < N) ? Ct[i * NS + n0 + a] * ei : 0.0f;
+                        yv[a] = dYs[i * PS + p0 + a];
+                    }
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(cv[a], yv[q], acc[a][q]);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    if (n0 + a >= N) break;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dG[(n0 + a) * PS + p0 + q] = fmaf(dec_end, dG[(n0 + a) * PS + p0 + q], acc[a][q]);
+                }
             }
         }
         __syncthreads();
