@@ -192,6 +192,27 @@ __device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
 __device__ __forceinline__ float rms_inv(float ss, float inv_n, float eps) {
     return rsqrtf(fmaxf(fmaf(ss, inv_n, eps), 1.17549435e-38f));
 }
+
+// 1 / RMS of a 64- or 128-element bf16 row held as two half rows in lanes l and
+// l ^ 16 (GPT 16-byte groups each): the squares summed in packed fp32 pairs on two
+// accumulators, so the dependent chain is GPT * 2 deep instead of GPT * 8.
+template <int GPT>
+__device__ __forceinline__ float row_rms_inv(const uint4 (&v)[GPT], float inv_n, float eps) {
+    float2 s0 = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int g = 0; g < GPT; ++g) {
+        const uint32_t pv[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+        float2 e0 = make_float2(bf_lo(pv[0]), bf_hi(pv[0])), e1 = make_float2(bf_lo(pv[1]), bf_hi(pv[1]));
+        float2 e2 = make_float2(bf_lo(pv[2]), bf_hi(pv[2])), e3 = make_float2(bf_lo(pv[3]), bf_hi(pv[3]));
+        s0 = __ffma2_rn(e0, e0, s0);
+        s1 = __ffma2_rn(e1, e1, s1);
+        s0 = __ffma2_rn(e2, e2, s0);
+        s1 = __ffma2_rn(e3, e3, s1);
+    }
+    float ss = (s0.x + s1.x) + (s0.y + s1.y);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    return rms_inv(ss, inv_n, eps);
+}
 // Byte offset of the 16-byte group g of row `row` in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(int row, int g) {
     return (uint32_t)(row * 128 + (((g & 7) ^ (row & 7)) << 4) + (g >> 3) * (kRows * 128));
@@ -249,18 +270,20 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     }
     if (tid < 2 * K) s_carry[tid] = 0.0f;
     if constexpr (NORM) {
-        // the scales and this head's biases: with the rotation wB | wC | bB | bC
-        // (float [4][N]); without it B and C interleaved per channel, (wB[n], wC[n])
-        // at 2 n and (bB[n], bC[n]) at 2 N + 2 n
+        // the scales and this head's biases: with the rotation per pair of channels
+        // (n, n + 1), (w[n], w[n + 1], b[n], b[n + 1]) at 2 n for B and at 2 N + 2 n
+        // for C; without it B and C interleaved per channel, (wB[n], wC[n]) at 2 n
+        // and (bB[n], bC[n]) at 2 N + 2 n
         float* nrm = reinterpret_cast<float*>(smem + CF::OFF_NRM);
         for (int i = tid; i < N; i += kThreads) {
             const float v[4] = {__ldg(prm.norm_wB + i), __ldg(prm.norm_wC + i), __ldg(prm.norm_bB + (int64_t)h * N + i),
                                 __ldg(prm.norm_bC + (int64_t)h * N + i)};
             if (ROT) {
-                nrm[i] = v[0];
-                nrm[N + i] = v[1];
-                nrm[2 * N + i] = v[2];
-                nrm[3 * N + i] = v[3];
+                const int o = 2 * (i & ~1) + (i & 1);
+                nrm[o] = v[0];
+                nrm[o + 2] = v[2];
+                nrm[2 * N + o] = v[1];
+                nrm[2 * N + o + 2] = v[3];
             } else {
                 nrm[2 * i] = v[0];
                 nrm[2 * i + 1] = v[1];
@@ -503,29 +526,23 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 // head's bias in fp32 and rounded to bf16 in place, before the angles
                 // (no sine or cosine is live yet).  The two halves of a row sit in lanes
                 // l and l ^ 16.
-                const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);   // wB | wC | bB | bC
+                const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);   // B's (w, w, b, b) per pair
                 uint8_t* sbn = st + CF::ST_B;
                 uint4 v[GPT];
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) v[g] = *reinterpret_cast<const uint4*>(sbn + swz(row, hf * GPT + g));
-                float ss = 0.0f;
-#pragma unroll
-                for (int g = 0; g < GPT; ++g) {
-                    const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v[g]);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pv[m]), bf_lo(pv[m]), fmaf(bf_hi(pv[m]), bf_hi(pv[m]), ss));
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                const float inv = rms_inv(ss, 1.0f / N, prm.norm_eps);
+                const float inv = row_rms_inv(v, 1.0f / N, prm.norm_eps);
+                const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
                 for (int g = 0; g < GPT; ++g) {
                     uint32_t* pv = reinterpret_cast<uint32_t*>(&v[g]);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const int n = (hf * GPT + g) * 8 + 2 * m;   // column of the pair's first element
-                        const float2 w = *reinterpret_cast<const float2*>(nrm + n);
-                        const float2 bi = *reinterpret_cast<const float2*>(nrm + 2 * N + n);
-                        pv[m] = pack_bf16(fmaf(bf_lo(pv[m]) * inv, w.x, bi.x), fmaf(bf_hi(pv[m]) * inv, w.y, bi.y));
+                        const float4 wb = *reinterpret_cast<const float4*>(nrm + 2 * n);
+                        const float2 u = __ffma2_rn(__fmul2_rn(make_float2(bf_lo(pv[m]), bf_hi(pv[m])), inv2),
+                                                    make_float2(wb.x, wb.y), make_float2(wb.z, wb.w));
+                        pv[m] = pack_bf16(u.x, u.y);
                     }
                     *reinterpret_cast<uint4*>(sbn + swz(row, hf * GPT + g)) = v[g];
                 }
@@ -582,17 +599,15 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     // the plain path: C's row sum of squares over one 16-byte group at a
                     // time, then per group normalise C, rotate B and C, store both
                     if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
-                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM);   // wB | wC | bB | bC
-                    float ss = 0.0f;
+                    const float* nrm = reinterpret_cast<const float*>(smem + CF::OFF_NRM) + 2 * N;   // C's
+                    float ic;
+                    {
+                        uint4 q[GPT];
 #pragma unroll
-                    for (int g = 0; g < GPT; ++g) {
-                        const uint4 q = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
-                        const uint32_t pq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) ss = fmaf(bf_lo(pq[m]), bf_lo(pq[m]), fmaf(bf_hi(pq[m]), bf_hi(pq[m]), ss));
+                        for (int g = 0; g < GPT; ++g) q[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
+                        ic = row_rms_inv(q, 1.0f / N, prm.norm_eps);
                     }
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                    const float ic = rms_inv(ss, 1.0f / N, prm.norm_eps);
+                    const float2 ic2 = make_float2(ic, ic);
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {
                         const uint32_t off = swz(row, hf * GPT + g);
@@ -602,12 +617,13 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int n = (hf * GPT + g) * 8 + 2 * m;
-                            const float2 w = *reinterpret_cast<const float2*>(nrm + N + n);
-                            const float2 bi = *reinterpret_cast<const float2*>(nrm + 3 * N + n);
+                            const float4 wb = *reinterpret_cast<const float4*>(nrm + 2 * n);
+                            const float2 cq = __ffma2_rn(__fmul2_rn(make_float2(bf_lo(pc[m]), bf_hi(pc[m])), ic2),
+                                                         make_float2(wb.x, wb.y), make_float2(wb.z, wb.w));
                             // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos), for the B pair
                             // and the normalised C pair at once: u = (a_B, a_C), v = (b_B, b_C)
-                            const float2 u = make_float2(bf_lo(pb[m]), fmaf(bf_lo(pc[m]) * ic, w.x, bi.x));
-                            const float2 v = make_float2(bf_hi(pb[m]), fmaf(bf_hi(pc[m]) * ic, w.y, bi.y));
+                            const float2 u = make_float2(bf_lo(pb[m]), cq.x);
+                            const float2 v = make_float2(bf_hi(pb[m]), cq.y);
                             const float co = cn[g * 4 + m], si = sn[g * 4 + m];
                             const float2 c2 = make_float2(co, co), s2 = make_float2(si, si), ns2 = make_float2(-si, -si);
                             const float2 u2 = __ffma2_rn(u, c2, __fmul2_rn(v, s2));
