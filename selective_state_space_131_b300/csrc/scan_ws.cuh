@@ -641,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     uint4 vc[GPT];
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) vc[g] = *reinterpret_cast<const uint4*>(scc + swz(row, hf * GPT + g));
-                    float2 ss = make_float2(0.0f, 0.0f);   // (B row, C row) sums of squares
+                    // (B row, C row) sums of squares on two accumulators (half the dependent chain)
+                    float2 ss = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {
                         const uint32_t* pb = reinterpret_cast<const uint32_t*>(&vb[g]);
@@ -650,9 +651,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                         for (int m = 0; m < 4; ++m) {
                             const float2 u = make_float2(bf_lo(pb[m]), bf_lo(pc[m]));
                             const float2 v = make_float2(bf_hi(pb[m]), bf_hi(pc[m]));
-                            ss = __ffma2_rn(u, u, __ffma2_rn(v, v, ss));
+                            ss = __ffma2_rn(u, u, ss);
+                            s1 = __ffma2_rn(v, v, s1);
                         }
                     }
+                    ss.x += s1.x;
+                    ss.y += s1.y;
                     // the tiles are unpacked again below rather than kept as 64 fp32 values
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {
