@@ -94,6 +94,11 @@ SMALL = [
     ("bf16", 130, 64, 64, 4, 16, True, True),
     ("bf16", 150, 64, 128, 1, 32, True, True),
     ("bf16", 100, 32, 16, 2, 32, True, False),
+    # state sizes that leave a partial 4-wide register tile (N % 4 == 2), narrow heads
+    ("f32", 77, 12, 6, 1, 16, True, True),
+    ("f32", 50, 4, 2, 2, 16, True, True),
+    ("f32", 90, 8, 10, 4, 16, True, True),
+    ("bf16", 81, 12, 6, 2, 32, True, True),
 ]
 
 

@@ -37,7 +37,10 @@ def run(m3, inp, chunk, expect_algo):
     return y.float().cpu(), fs.cpu()
 
 
-@pytest.mark.parametrize("R,N,P", [(1, 16, 16), (2, 64, 32), (4, 32, 64)], ids=lambda v: str(v))
+# (N = 6 and 10 leave a partial 4-wide register tile of state rows; P = 12 and 4
+# give 3 and 1 column tiles)
+@pytest.mark.parametrize("R,N,P", [(1, 16, 16), (2, 64, 32), (4, 32, 64), (1, 6, 12), (2, 10, 4)],
+                         ids=lambda v: str(v))
 def test_chunk_invariance_f32(m3, R, N, P):
     """Chunks of 16, 32, 64, 128 tokens over T = 300 (ragged for every chunk):
     each within 1e-4 of the oracle, so within 2e-4 of each other."""
