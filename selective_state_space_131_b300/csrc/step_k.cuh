@@ -250,15 +250,15 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
             float xr[R][4];
 #pragma unroll
             for (int r = 0; r < R; ++r) SVec<T>::ld4(cur + (r * P + p0) * es, xr[r]);
-            float yp[R][4];
+            // the four columns in two packed fp32 pairs (each lane's arithmetic that of the
+            // scalar form, so the same bits)
+            float2 yp[R][2];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int jx = 0; jx < 4; ++jx) yp[r][jx] = 0.0f;
+            for (int r = 0; r < R; ++r) yp[r][0] = yp[r][1] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int m = 0; m < kRPT / 2; ++m) {
-                float* h0 = reinterpret_cast<float*>(&hs[2 * m]);
-                float* h1 = reinterpret_cast<float*>(&hs[2 * m + 1]);
+                float2* h0 = reinterpret_cast<float2*>(&hs[2 * m]);
+                float2* h1 = reinterpret_cast<float2*>(&hs[2 * m + 1]);
                 float2 br[R], cr[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -266,21 +266,26 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                     cr[r] = SVec<T>::ld2(cur + a.xb + a.nb + (r * N + n0 + 2 * m) * es);
                 }
                 const float ac = cf[2 * m], as = cf[2 * m + 1];
+                const float2 ac2 = make_float2(ac, ac), as2 = make_float2(as, as), nas2 = make_float2(-as, -as);
+                const float2 g2 = make_float2(gc.x, gc.x), c2 = make_float2(gc.y, gc.y);
 #pragma unroll
-                for (int jx = 0; jx < 4; ++jx) {
-                    float u0 = 0.0f, u1 = 0.0f;
+                for (int hv = 0; hv < 2; ++hv) {
+                    float2 u0 = make_float2(0.0f, 0.0f), u1 = make_float2(0.0f, 0.0f);
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        u0 = fmaf(br[r].x, xr[r][jx], u0);
-                        u1 = fmaf(br[r].y, xr[r][jx], u1);
+                        const float2 xv = make_float2(xr[r][2 * hv], xr[r][2 * hv + 1]);
+                        u0 = __ffma2_rn(make_float2(br[r].x, br[r].x), xv, u0);
+                        u1 = __ffma2_rn(make_float2(br[r].y, br[r].y), xv, u1);
                     }
                     // alpha Rot(theta) g + gamma u: (a, b) -> (ac a - as b, as a + ac b)
-                    const float o0 = fmaf(gc.x, u0, fmaf(ac, h0[jx], -as * h1[jx]));
-                    const float o1 = fmaf(gc.x, u1, fmaf(as, h0[jx], ac * h1[jx]));
+                    const float2 o0 = __ffma2_rn(g2, u0, __ffma2_rn(ac2, h0[hv], __fmul2_rn(nas2, h1[hv])));
+                    const float2 o1 = __ffma2_rn(g2, u1, __ffma2_rn(as2, h0[hv], __fmul2_rn(ac2, h1[hv])));
 #pragma unroll
-                    for (int r = 0; r < R; ++r) yp[r][jx] = fmaf(cr[r].x, o0, fmaf(cr[r].y, o1, yp[r][jx]));
-                    h0[jx] = upd ? fmaf(gc.y, u0, o0) : o0;
-                    h1[jx] = upd ? fmaf(gc.y, u1, o1) : o1;
+                    for (int r = 0; r < R; ++r)
+                        yp[r][hv] = __ffma2_rn(make_float2(cr[r].x, cr[r].x), o0,
+                                               __ffma2_rn(make_float2(cr[r].y, cr[r].y), o1, yp[r][hv]));
+                    h0[hv] = upd ? __ffma2_rn(c2, u0, o0) : o0;
+                    h1[hv] = upd ? __ffma2_rn(c2, u1, o1) : o1;
                 }
             }
             // y of token j: lanes P4 apart, then the warps through shared memory
@@ -289,13 +294,16 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
 #pragma unroll
                 for (int r = 0; r < R; ++r)
 #pragma unroll
-                    for (int jx = 0; jx < 4; ++jx) yp[r][jx] += __shfl_xor_sync(0xffffffffu, yp[r][jx], o);
+                    for (int hv = 0; hv < 2; ++hv) {
+                        yp[r][hv].x += __shfl_xor_sync(0xffffffffu, yp[r][hv].x, o);
+                        yp[r][hv].y += __shfl_xor_sync(0xffffffffu, yp[r][hv].y, o);
+                    }
             float* rb = red + (j & 1) * nwarps * R * P;
             if (lane < P4) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     *reinterpret_cast<float4*>(rb + (warp * R + r) * P + p0) =
-                        make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
+                        make_float4(yp[r][0].x, yp[r][0].y, yp[r][1].x, yp[r][1].y);
             }
             __syncthreads();
             const int64_t tj = (b * a.k + j) * H + h;
