@@ -229,10 +229,7 @@ int launch_step_ring(const m3_dims* d, float* state, const void* x_t, const floa
     return launch_status();
 }
 
-// The tensor-core kernel takes its shapes when the chunk is one 64-row tile
-// (Q R = 64); every other chunk runs on the chunked CUDA-core kernel when its
-// shared memory fits, else on the token-serial kernel.
-// The multi-token decode kernel for the common shapes (step_fast.cuh); every
+// The multi-token decode kernel for the common shapes (step_k.cuh); every
 // tensor it reads with vector loads is 16-byte aligned (checked by the caller).
 template <typename T>
 int launch_step_k(const m3_dims* d, float* state, const void* x, const float* dt, const float* A, const void* B,
@@ -266,6 +263,9 @@ int launch_step_k(const m3_dims* d, float* state, const void* x, const float* dt
     return launch_status();
 }
 
+// The tensor-core kernel takes its shapes when the chunk is one 64-row tile
+// (Q R = 64); every other chunk runs on the chunked CUDA-core kernel when its
+// shared memory fits, else on the token-serial kernel.
 int scan_algorithm(const m3_dims* d) {
     if (check_dims(d, true) != M3_OK) return M3_ALGO_NONE;
     if (m3ws::supports(*d) && d->chunk * d->rank == m3ws::kRows) return M3_ALGO_CHUNKED_TC;

@@ -1,6 +1,7 @@
 """GPU parity of the multi-token decode step (m3_step_k: k tokens per launch,
 the state read and written once) against the fp64 oracle, through the C ABI:
-the fast kernel's shapes with fp32 and bf16 inputs for several k, missing
+the fast kernel's shapes with fp32 and bf16 inputs for several k (and launches
+of up to 70 tokens), missing
 optional inputs, equality with k single steps, the generic fallback (shapes the
 kernel does not take, and element-aligned inputs), and the decode workload
 (b256 h32 P64 N64 fp32) over 1024 tokens as 128 launches of 8, checked every
@@ -62,6 +63,18 @@ def test_step_k_matches_oracle(m3, P, N, R, k, dtype):
     yr, fr = oracle_k(toks, s0, pB, pX)
     ey, es = max_rel(y, yr), max_rel(st, fr)
     assert ey <= TOL[dtype] and es <= TOL[dtype], (ey, es)
+
+
+@pytest.mark.parametrize("k", [31, 32, 33, 70])
+@pytest.mark.parametrize("R,dtype", [(1, "f32"), (4, "f32"), (2, "bf16")])
+def test_step_k_long_launches(m3, k, R, dtype):
+    """Launches longer than one group of 8 staged tokens, ragged and not: the
+    next group loads while one runs, the state stays in registers across
+    groups.  Same bar."""
+    toks, s0, pB, pX = make_case(3, 5, 64, 64, R, k, dtype, 770 + k + R)
+    y, st = run_k(m3, toks, s0, pB, pX)
+    yr, fr = oracle_k(toks, s0, pB, pX)
+    assert max_rel(y, yr) <= TOL[dtype] and max_rel(st, fr) <= TOL[dtype]
 
 
 @pytest.mark.parametrize("prev,lam,theta", [(False, True, True), (True, False, True), (True, True, False),
