@@ -2,7 +2,7 @@
 """Benchmark of the Mamba-3 scan on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1|2|3] [--no-decode] [--no-cpu-baseline]
+                    [--workload NAME] [--no-decode] [--no-cpu-baseline]
 
 One step = one chunked prefill (m3_scan_fwd) over one batch of the workload,
 inputs resident in HBM (1.2 GB for the default workload, larger than the
@@ -162,10 +162,10 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0][1], "reasons": reasons, "samples": len(rows)}
 
 
-def rank_seed(workload: int, rank: int) -> int:
+def rank_seed(seed: int, rank: int) -> int:
     """Input seed of one rank: every rank draws its own copy of the workload
     (independent (batch, head) sequences, weak scaling, no data exchanged)."""
-    return workload + 1000 * rank
+    return seed + 1000 * rank
 
 
 def max_over_ranks(ms: float, world: int, device="cpu") -> float:
@@ -219,7 +219,7 @@ def run_reference(args, shape, cfg_name):
     if rank != 0:
         return None
     # size each step's sample so that warm-up + steps fit the wall budget
-    full, _ = oracle_sample(shape, args.workload, args.ref_units)
+    full, _ = oracle_sample(shape, inputs.WORKLOAD_SEEDS[args.workload], args.ref_units)
     one = {k: (None if v is None else (v[:1] if k == "A" else v[:, :, :1])) for k, v in full.items()}
     _, sec1, thr = time_cpu_oracle(shape, one, 1)
     n_steps = args.warmup + args.steps
@@ -260,7 +260,7 @@ def bench_decode_k(m3, stream, steps: int, rank_seed: int, rank: int, k: int):
     m3_step_k launches of k tokens each (the state read and written once per
     launch), captured in one CUDA graph and replayed on `stream`."""
     launches = steps // k
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": launches * k, "rank": rank})
+    shape = inputs.DecodeShape(**{**inputs.WORKLOADS[inputs.DECODE].__dict__, "steps": launches * k, "rank": rank})
     dec = inputs.make_decode_inputs(shape, 4 + rank_seed, device="cuda")
     b, H = shape.batch, shape.heads
     lay = lambda a: a[1:].reshape(launches, k, b, H, *a.shape[3:]).transpose(1, 2).contiguous()
@@ -302,7 +302,7 @@ def bench_decode_k(m3, stream, steps: int, rank_seed: int, rank: int, k: int):
     nbytes = decode_k_bytes(shape, k)
     del X, DT, Bm, Cm, LAM, TH, Y, state, g, prevs
     torch.cuda.empty_cache()
-    return {"workload": inputs.CONFIG_NAMES[4] + f"_R{rank}_k{k}", "tokens_per_launch": k,
+    return {"workload": inputs.DECODE + f"_R{rank}_k{k}", "tokens_per_launch": k,
             "us_per_launch": ms * 1e3, "tokens_per_s": b * k * 1e3 / ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9,
             "bytes_per_launch": nbytes, "graph_launches": launches, "entry": "m3_step_k"}
 
@@ -311,7 +311,7 @@ def bench_decode(m3, stream, steps: int, rank_seed: int, rank: int = 1):
     """Decode sweep of the decode workload (fp32, b256 h32 P64 N64, rank R):
     `steps` consecutive m3_step calls captured in one CUDA graph and replayed
     on `stream` (the stream the events are recorded on); returns a dict."""
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "steps": steps, "rank": rank})
+    shape = inputs.DecodeShape(**{**inputs.WORKLOADS[inputs.DECODE].__dict__, "steps": steps, "rank": rank})
     inp = inputs.make_decode_inputs(shape, 4 + rank_seed, device="cuda")
     state = inp["state0"].clone()
     ys = torch.empty_like(inp["x"][1:])
@@ -345,7 +345,7 @@ def bench_decode(m3, stream, steps: int, rank_seed: int, rank: int = 1):
     nbytes = decode_bytes(shape)
     del inp, ys, state, g
     torch.cuda.empty_cache()
-    return {"workload": inputs.CONFIG_NAMES[4] + f"_R{rank}", "steps_per_s": 1e3 / ms, "us_per_step": ms * 1e3,
+    return {"workload": inputs.DECODE + f"_R{rank}", "steps_per_s": 1e3 / ms, "us_per_step": ms * 1e3,
             "tokens_per_s": shape.batch * 1e3 / ms, "GB_per_s": nbytes / (ms * 1e-3) / 1e9,
             "bytes_per_step": nbytes, "graph_steps": steps, "launches_per_step": 1}
 
@@ -445,7 +445,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3])
+    ap.add_argument("--workload", default=inputs.SISO, choices=list(inputs.PREFILL_WORKLOADS))
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -457,16 +457,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="wall time the cpu_baseline repeats for")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling captures)")
     ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen (profiling captures)")
+    ap.add_argument("--chunk", type=int, default=0, help="override the workload's chunk (profiling captures)")
     ap.add_argument("--no-other", action="store_true", help="skip the other prefill workloads")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward pass")
     ap.add_argument("--decode-only", action="store_true", help="only the decode sweep (profiling captures)")
     args = ap.parse_args()
 
-    shape = inputs.CONFIGS[args.workload]
-    if args.batch or args.seqlen:
+    shape = inputs.WORKLOADS[args.workload]
+    wseed = inputs.WORKLOAD_SEEDS[args.workload]
+    if args.batch or args.seqlen or args.chunk:
         shape = inputs.ScanShape(**{**shape.__dict__, "batch": args.batch or shape.batch,
-                                    "seqlen": args.seqlen or shape.seqlen})
-    cfg_name = inputs.CONFIG_NAMES[args.workload]
+                                    "seqlen": args.seqlen or shape.seqlen, "chunk": args.chunk or shape.chunk})
+    cfg_name = args.workload
     world, rank, local = dist_env()
 
     if args.impl == "reference":
@@ -489,7 +491,7 @@ def main():
                   flush=True)
         return 0
 
-    inp = inputs.make_scan_inputs(shape, rank_seed(args.workload, rank))
+    inp = inputs.make_scan_inputs(shape, rank_seed(wseed, rank))
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     b, T, H, R, P = d["x"].shape
     N = d["B"].shape[-1]
@@ -591,10 +593,10 @@ def main():
     if not args.no_other and rank == 0:
         # the other prefill workloads, same protocol (reported beside the headline)
         other = {}
-        for w in (1, 2, 3):
+        for w in inputs.PREFILL_WORKLOADS:
             if w == args.workload:
                 continue
-            sh = inputs.CONFIGS[w]
+            sh = inputs.WORKLOADS[w]
             note = None
             if sh.chunk * sh.rank != 64:
                 # the tensor-core kernel's chunk is one 64-row tile: 64 / R tokens (16 at
@@ -602,20 +604,20 @@ def main():
                 note = (f"chunk {64 // sh.rank} executed (the 64-row tensor-core tile at R = {sh.rank}); "
                         f"chunk {sh.chunk} runs on the CUDA-core chunked kernel")
                 sh = inputs.ScanShape(**{**sh.__dict__, "chunk": 64 // sh.rank})
-            wms = time_prefill(m3, stream, sh, w, dev, steps=20, warmup=3)
+            wms = time_prefill(m3, stream, sh, inputs.WORKLOAD_SEEDS[w], dev, steps=20, warmup=3)
             wb = scan_bytes(sh)
-            other[inputs.CONFIG_NAMES[w]] = {
+            other[w] = {
                 "ms_per_step": wms, "tokens_per_s": sh.batch * sh.seqlen / (wms * 1e-3),
                 "GB_per_s": wb / (wms * 1e-3) / 1e9, "hbm_frac": wb / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "algorithmic_bytes": wb, "chunk": sh.chunk,
                 "tensor_tflops": scan_flops(sh) / (wms * 1e-3) / 1e12}
             if note:
-                other[inputs.CONFIG_NAMES[w]]["note"] = note
+                other[w]["note"] = note
         # the timed workload again with the B / C normalisation and biases fused
         # into the prologue (m3_scan_fwd_bcnorm; the parameters add 1 KB per head)
-        wms = time_prefill(m3, stream, shape, args.workload, dev, steps=20, warmup=3, bcnorm=True)
+        wms = time_prefill(m3, stream, shape, wseed, dev, steps=20, warmup=3, bcnorm=True)
         wb = scan_bytes(shape)
-        other[inputs.CONFIG_NAMES[args.workload] + "_bcnorm"] = {
+        other[args.workload + "_bcnorm"] = {
             "ms_per_step": wms, "tokens_per_s": shape.batch * shape.seqlen / (wms * 1e-3),
             "GB_per_s": wb / (wms * 1e-3) / 1e9, "hbm_frac": wb / (wms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": wb}
@@ -623,7 +625,7 @@ def main():
 
     if not args.no_bwd and rank == 0:
         # the backward pass of the timed workload (training): m3_scan_bwd
-        bms, wsb = time_bwd(m3, stream, shape, args.workload, dev, steps=10, warmup=3)
+        bms, wsb = time_bwd(m3, stream, shape, wseed, dev, steps=10, warmup=3)
         bb = bwd_bytes(shape)
         result["backward"] = {
             "workload": cfg_name, "entry": "m3_scan_bwd", "ms_per_step": bms,
@@ -653,7 +655,7 @@ def main():
         # the oracle on every host core: the workload's first batch rows (all
         # heads, full T), repeated until about args.cpu_seconds of wall time
         import oracle
-        full = inputs.make_scan_inputs(shape, args.workload)
+        full = inputs.make_scan_inputs(shape, wseed)
         rows = max(1, min(shape.batch, args.cpu_rows))
         sample = {k: (None if v is None else (v if k == "A" else v[:rows].contiguous())) for k, v in full.items()}
         del full

@@ -50,22 +50,23 @@ class DecodeShape:
     dtype: str = "f32"
 
 
-# The five workloads: four prefill scans and the decode sweep.
-CONFIGS = {
-    0: ScanShape(batch=1, seqlen=256, heads=2, headdim=16, dstate=16, rank=1, chunk=32, dtype="f32"),
-    1: ScanShape(batch=8, seqlen=4096, heads=32, headdim=64, dstate=128, rank=1, chunk=64, dtype="bf16",
-                 with_lambda=False, with_theta=False),
-    2: ScanShape(batch=8, seqlen=8192, heads=32, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16"),
-    3: ScanShape(batch=8, seqlen=4096, heads=32, headdim=64, dstate=64, rank=4, chunk=64, dtype="bf16"),
-    4: DecodeShape(batch=256, heads=32, headdim=64, dstate=64, rank=1, steps=1024, dtype="f32"),
+# The five workloads, by name: four prefill scans and the decode sweep.
+TINY = "tiny_siso_f32_b1h2T256P16N16"
+SSD_EQUIV = "ssd_equiv_bf16_b8h32T4096P64N128"
+SISO = "m3_siso_bf16_b8h32T8192P64N64"
+MIMO = "m3_mimo_r4_bf16_b8h32T4096P64N64"
+DECODE = "decode_f32_b256h32P64N64"
+WORKLOADS = {
+    TINY: ScanShape(batch=1, seqlen=256, heads=2, headdim=16, dstate=16, rank=1, chunk=32, dtype="f32"),
+    SSD_EQUIV: ScanShape(batch=8, seqlen=4096, heads=32, headdim=64, dstate=128, rank=1, chunk=64, dtype="bf16",
+                         with_lambda=False, with_theta=False),
+    SISO: ScanShape(batch=8, seqlen=8192, heads=32, headdim=64, dstate=64, rank=1, chunk=64, dtype="bf16"),
+    MIMO: ScanShape(batch=8, seqlen=4096, heads=32, headdim=64, dstate=64, rank=4, chunk=64, dtype="bf16"),
+    DECODE: DecodeShape(batch=256, heads=32, headdim=64, dstate=64, rank=1, steps=1024, dtype="f32"),
 }
-CONFIG_NAMES = {
-    0: "tiny_siso_f32_b1h2T256P16N16",
-    1: "ssd_equiv_bf16_b8h32T4096P64N128",
-    2: "m3_siso_bf16_b8h32T8192P64N64",
-    3: "m3_mimo_r4_bf16_b8h32T4096P64N64",
-    4: "decode_f32_b256h32P64N64",
-}
+# the base seed of each workload's synthetic inputs
+WORKLOAD_SEEDS = {TINY: 0, SSD_EQUIV: 1, SISO: 2, MIMO: 3, DECODE: 4}
+PREFILL_WORKLOADS = (SSD_EQUIV, SISO, MIMO)
 
 
 def _head_params(g, heads, K, device):

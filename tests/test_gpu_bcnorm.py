@@ -76,7 +76,7 @@ def test_bcnorm_small(m3, T, N, R, lam, th):
 def test_bcnorm_siso_workload_full_size(m3):
     """The SISO complex + trapezoidal workload (b8 h32 T8192 P64 N64) with the
     normalisation, on 64 sequences: every batch row, eight heads."""
-    ey, ef = run_and_check(m3, inputs.CONFIGS[2], 2, bsel=list(range(8)), hsel=[0, 4, 9, 13, 18, 22, 27, 31])
+    ey, ef = run_and_check(m3, inputs.WORKLOADS[inputs.SISO], 2, bsel=list(range(8)), hsel=[0, 4, 9, 13, 18, 22, 27, 31])
     print(f"full size: y {ey:.2e} state {ef:.2e}")
 
 

@@ -139,7 +139,7 @@ def test_bwd_siso_workload_full_size(m3):
     """The SISO complex + trapezoidal workload (b8 h32 T8192 P64 N64, bf16) at
     full size -- the launch the bench times -- checked on three heads for every
     batch row (24 sequences; dA[h] sums all eight rows of a head)."""
-    shape = inputs.CONFIGS[2]
+    shape = inputs.WORKLOADS[inputs.SISO]
     inp = inputs.make_scan_inputs(shape, 2)
     dy, dfinal = upstream(shape, 892)
     got = gpu_bwd(m3, inp, dy, dfinal, 64)

@@ -88,7 +88,7 @@ def test_mimo_workload_chunk64_full_size(m3):
     """The MIMO R = 4 workload (b8 h32 T4096 P64 N64, bf16) at its stated chunk
     of 64 tokens: 256-row chunks on the chunked CUDA-core kernel, checked on
     every batch row for eight heads (64 sequences)."""
-    shape = inputs.CONFIGS[3]
+    shape = inputs.WORKLOADS[inputs.MIMO]
     assert shape.chunk == 64 and shape.rank == 4
     inp = inputs.make_scan_inputs(shape, 3)
     y, fs = run(m3, inp, 64, m3.M3_ALGO_CHUNKED_SIMT)

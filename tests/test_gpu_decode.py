@@ -134,7 +134,7 @@ def test_decode_workload_full_size(m3, R):
     """The decode workload (b256 h32 P64 N64, fp32 state and inputs) at full
     size, the launch the bench times, over 16 consecutive steps; checked on
     sampled (batch, head) units."""
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "rank": R, "steps": 16})
+    shape = inputs.DecodeShape(**{**inputs.WORKLOADS[inputs.DECODE].__dict__, "rank": R, "steps": 16})
     ey, es = run_chain(m3, shape, 4, 16, sel=([0, 100, 255], [0, 17, 31]))
     assert ey <= 1e-4 and es <= 1e-4, (ey, es)
 
@@ -147,7 +147,7 @@ def test_decode_sweep_1024_steps_in_graph(m3, R):
     (batch, head) units; the oracle runs the same 1024 tokens in 64-token
     segments, each started from its own previous segment's final state."""
     steps, seg = 1024, 64
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "rank": R, "steps": steps})
+    shape = inputs.DecodeShape(**{**inputs.WORKLOADS[inputs.DECODE].__dict__, "rank": R, "steps": steps})
     inp = inputs.make_decode_inputs(shape, 4 + R, device="cuda")
     bsel, hsel = [0, 37, 128, 255], [0, 11, 31]
     state = inp["state0"].clone()

@@ -37,7 +37,7 @@ def check_scan(m3, shape, seed, expect_algo=None):
 def test_config0_tiny_f32(m3):
     """The tiny SISO fp32 workload (b1 h2 T256 P16 N16, seed 0) at 1e-4, in
     chunks of 32 tokens on the chunked CUDA-core kernel."""
-    ey, ef = check_scan(m3, inputs.CONFIGS[0], 0, m3.M3_ALGO_CHUNKED_SIMT)
+    ey, ef = check_scan(m3, inputs.WORKLOADS[inputs.TINY], 0, m3.M3_ALGO_CHUNKED_SIMT)
     print(f"config0: y {ey:.2e} state {ef:.2e}")
 
 

@@ -151,7 +151,7 @@ def test_step_k_decode_workload_1024_tokens(m3, R):
     y and the state checked after every 64 tokens on 12 sampled units."""
     k, launches, seg = 8, 128, 64
     steps = k * launches
-    shape = inputs.DecodeShape(**{**inputs.CONFIGS[4].__dict__, "rank": R, "steps": steps})
+    shape = inputs.DecodeShape(**{**inputs.WORKLOADS[inputs.DECODE].__dict__, "rank": R, "steps": steps})
     dec = inputs.make_decode_inputs(shape, 40 + R, device="cuda")
     b, H = shape.batch, shape.heads
     # tokens 1..steps in launch-major, token-major order: [launch, b, k, h, ...]

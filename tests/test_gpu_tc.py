@@ -75,21 +75,21 @@ def test_tc_small(m3, T, N, R, lam, th):
 # SISO workloads; for the MIMO workload every batch row on 17 of the 32 heads
 # (136 of 256 sequences).  With 256 CTAs on 148 SMs some SMs run one CTA and
 # others two, so both placements are among the units checked.
-FULL_SEL = {1: (list(range(8)), list(range(32))),
-            2: (list(range(8)), list(range(32))),
-            3: (list(range(8)), list(range(0, 32, 2)) + [31])}
+FULL_SEL = {inputs.SSD_EQUIV: (list(range(8)), list(range(32))),
+            inputs.SISO: (list(range(8)), list(range(32))),
+            inputs.MIMO: (list(range(8)), list(range(0, 32, 2)) + [31])}
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3])
-def test_tc_full_size_workloads(m3, cfg):
+@pytest.mark.parametrize("name", list(inputs.PREFILL_WORKLOADS))
+def test_tc_full_size_workloads(m3, name):
     """The bf16 workloads at full size, in the launch configuration the bench
     times (the tensor-core kernel; for the MIMO workload its 16-token chunk, the
     64-row tile at R = 4), checked against the oracle on the units of FULL_SEL."""
-    shape = inputs.CONFIGS[cfg]
+    shape = inputs.WORKLOADS[name]
     shape = inputs.ScanShape(**{**shape.__dict__, "chunk": 64 // shape.rank})
-    bsel, hsel = FULL_SEL[cfg]
-    ey, ef = run_and_check(m3, shape, cfg, bsel, hsel)
-    print(f"config {cfg}: y {ey:.2e} state {ef:.2e}")
+    bsel, hsel = FULL_SEL[name]
+    ey, ef = run_and_check(m3, shape, inputs.WORKLOAD_SEEDS[name], bsel, hsel)
+    print(f"{name}: y {ey:.2e} state {ef:.2e}")
 
 
 def test_chunk_invariance_across_kernels(m3):
