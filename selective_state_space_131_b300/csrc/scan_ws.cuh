@@ -224,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                       const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_th,
                       const __grid_constant__ CUtensorMap map_y, const Params prm) {
     using CF = Cfg<NSLAB, R, ROT, NORM>;
+    // CKPT: the backward pass's checkpoint run, which needs the chunk states and
+    // angles only: S, the mask, Y_intra, Y_inter, the output and C's rotation are
+    // skipped (C is still loaded, so the copies keep one protocol)
+    static_assert(!(CKPT && NORM), "no checkpoint run with the fused normalisation");
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                                                        th_lo + k16 * (CF::TH_K16 >> 4), id_phi, k16 > 0);
                 ptx::umma_commit(&bar_phi);
             }
-            if (c >= 2 || (c == 1 && (prm.h0 != nullptr || prm.prev_B != nullptr))) {
+            if (!CKPT && (c >= 2 || (c == 1 && (prm.h0 != nullptr || prm.prev_B != nullptr)))) {
                 // Y_inter(c-1) = C~_{c-1} G_{c-2} (G: bf16 [N][P] rows, MN-major; G_{-1}
                 // is the continuation's initial state)
                 const uint32_t c_lo =
@@ -689,6 +693,21 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                         *reinterpret_cast<uint4*>(scc + off) = vc[g];
                         asm volatile("" ::: "memory");   // the next group's scale / bias loads stay behind
                     }
+                } else if (ROT && CKPT) {
+                    // B~ alone, kept in registers for B~' (S is not formed); x must be in
+                    // before dG
+                    if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
+#pragma unroll
+                    for (int g = 0; g < GPT; ++g) {
+                        uint32_t* pb = reinterpret_cast<uint32_t*>(&vb[g]);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
+                            const float a = bf_lo(pb[m]), bb = bf_hi(pb[m]);
+                            const float co = cn[g * 4 + m], si = sn[g * 4 + m];
+                            pb[m] = pack_bf16(fmaf(a, co, bb * si), fmaf(bb, co, a * -si));
+                        }
+                    }
                 } else if (ROT) {
                     if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
                     uint4 vc[GPT];
@@ -749,10 +768,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     constexpr uint32_t id_s = ptx::idesc_bf16(kRows, kRows, false, false);
                     constexpr uint32_t id_g = ptx::idesc_bf16(N, kP, true, true);
                     const uint32_t tm_s = tmem + CF::TM_SY0 + 64u * s;
+                    if constexpr (!CKPT) {
 #pragma unroll
-                    for (int k16 = 0; k16 < N / 16; ++k16) {   // K = state (K-major slabs)
-                        const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
-                        ptx::umma_bf16_lo<kDescHi, kDescHi>(tm_s, c_lo + ko, b_lo + ko, id_s, k16 > 0);
+                        for (int k16 = 0; k16 < N / 16; ++k16) {   // K = state (K-major slabs)
+                            const uint32_t ko = ((k16 >> 2) * TILE + (k16 & 3) * 32) >> 4;
+                            ptx::umma_bf16_lo<kDescHi, kDescHi>(tm_s, c_lo + ko, b_lo + ko, id_s, k16 > 0);
+                        }
                     }
 #pragma unroll
                     for (int k16 = 0; k16 < kRows / 16; ++k16)   // K = rows (MN-major operands)
@@ -763,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }
             __syncwarp();   // as above, for the S / dG issuer's warp
         }
-        if (tid == kEarlyIssuer && !aborted && (nch >= 2 || prm.h0 != nullptr || prm.prev_B != nullptr))
+        if (!CKPT && tid == kEarlyIssuer && !aborted && (nch >= 2 || prm.h0 != nullptr || prm.prev_B != nullptr))
             issue_early(nch);   // Y_inter(nch - 1)
         if (warp == 0) ptx::cp_async_wait_all();   // a stop may leave a scalar copy in flight
     } else {
@@ -798,6 +819,20 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 issue_loads_a(c + 2);
                 last_a = c + 2;
             }
+            if constexpr (CKPT) {
+                // nothing reads C, and x is free once dG_c is done: the rest of chunk c + 2
+                if (tid == kLoader && !fail && c + 2 < nch) {
+                    if (ROT) {
+                        issue_loads_b(c + 2);
+                        last_b = c + 2;
+                    } else {
+                        issue_loads_a(c + 2);
+                        last_a = c + 2;
+                    }
+                }
+            }
+            const float cs_i = sc[CF::SC_CS + ti];
+            if constexpr (!CKPT) {
             // S_c, block J (columns 16 J + [0, 16)) in v[8 J, 8 J + 8): this thread
             // holds columns 16 J + 8 hc + [0, 8) (waited for in the mask below)
             uint32_t v[32];
@@ -806,7 +841,6 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             // (2) mask: S' = S o M for this thread's row, 8 columns in each of the
             //     four 16-row blocks; the block kind (below / diagonal / above)
             //     is the same for the whole warp
-            const float cs_i = sc[CF::SC_CS + ti];
             {
                 constexpr int TB = CF::TB;
                 constexpr int TPC = 8 / R;                         // tokens under 8 columns
@@ -858,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                     *reinterpret_cast<uint4*>(t_sp + swz(i_row, 2 * J + hc)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
+            }   // !CKPT
             // (3) G_c = exp(cs_end) G_{c-1} + dG_c (fp32)
             if constexpr (CKPT) {
                 // G_{c-1} for the backward pass (rows and columns as held here)
@@ -901,6 +936,11 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (fail) { m3::set_status(m3::kStatusWaitTimeout); abort_s = 1; }
             if (ptx::bar_sync_or(kBarWG1, kWG, fail || abort_s)) { aborted = true; break; }
             if (leader) ptx::mbar_arrive(&bar_dgfree);
+            if constexpr (CKPT) {
+                // no output: the S/Y buffer of stage s (it held Phi_c only) is free
+                if (leader) ptx::mbar_arrive(&bar_syfree[s]);
+                continue;
+            }
             if (tid == kYIssuer) {
                 ptx::tc_fence_after();
                 // Y_intra = S' X -> TMEM S/Y[s] (S has been read by every thread)
