@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                       const __grid_constant__ CUtensorMap map_y, const Params prm) {
     using CF = Cfg<NSLAB, R, ROT, NORM>;
     // CKPT: the backward pass's checkpoint run, which needs the chunk states and
-    // angles only: S, the mask, Y_intra, Y_inter, the output and C's rotation are
-    // skipped (C is still loaded, so the copies keep one protocol)
+    // angles only: C is not loaded, and S, the mask, Y_intra, Y_inter and the
+    // output are skipped
     static_assert(!(CKPT && NORM), "no checkpoint run with the fused normalisation");
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -360,12 +360,13 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         const int s = c & 1;
         uint8_t* st = smem + s * CF::ST_BYTES;
         const int t0 = c * Q;
-        ptx::mbar_arrive_expect_tx(&bar_lda[s], CF::TX_A);
+        // (the checkpoint run reads no C)
+        ptx::mbar_arrive_expect_tx(&bar_lda[s], CF::TX_A - ((CKPT && !ROT) ? NSLAB * TILE : 0u));
         if (ROT) ptx::tma_load_4d(st + CF::ST_TH, &map_th, &bar_lda[s], 0, h, t0, b);
 #pragma unroll
         for (int sl = 0; sl < NSLAB; ++sl) {
             ptx::tma_load_5d(st + CF::ST_B + sl * TILE, &map_B, &bar_lda[s], sl * 64, 0, h, t0, b);
-            if (!ROT) ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_lda[s], sl * 64, 0, h, t0, b);
+            if (!ROT && !CKPT) ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_lda[s], sl * 64, 0, h, t0, b);
         }
         if (!ROT) ptx::tma_load_5d(st + CF::ST_X, &map_x, &bar_lda[s], 0, 0, h, t0, b);
     };
@@ -374,10 +375,12 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         const int s = c & 1;
         uint8_t* st = smem + s * CF::ST_BYTES;
         const int t0 = c * Q;
-        ptx::mbar_arrive_expect_tx(&bar_ldb[s], CF::TX_B);
+        ptx::mbar_arrive_expect_tx(&bar_ldb[s], CF::TX_B - (CKPT ? NSLAB * TILE : 0u));
+        if (!CKPT) {
 #pragma unroll
-        for (int sl = 0; sl < NSLAB; ++sl)
-            ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_ldb[s], sl * 64, 0, h, t0, b);
+            for (int sl = 0; sl < NSLAB; ++sl)
+                ptx::tma_load_5d(st + CF::ST_C + sl * TILE, &map_C, &bar_ldb[s], sl * 64, 0, h, t0, b);
+        }
         ptx::tma_load_5d(st + CF::ST_X, &map_x, &bar_ldb[s], 0, 0, h, t0, b);
     };
     int last_a = -1, last_b = -1;   // thread kLoader only: the last chunk of each part loaded
@@ -696,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 } else if (ROT && CKPT) {
                     // B~ alone, kept in registers for B~' (S is not formed); x must be in
                     // before dG
-                    if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // C and x
+                    if (!fail) fail = !ptx::mbar_wait(&bar_ldb[s], (c >> 1) & 1, kWaitBudget);   // x
 #pragma unroll
                     for (int g = 0; g < GPT; ++g) {
                         uint32_t* pb = reinterpret_cast<uint32_t*>(&vb[g]);
@@ -820,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
                 last_a = c + 2;
             }
             if constexpr (CKPT) {
-                // nothing reads C, and x is free once dG_c is done: the rest of chunk c + 2
+                // x is free once dG_c is done: the rest of chunk c + 2
                 if (tid == kLoader && !fail && c + 2 < nch) {
                     if (ROT) {
                         issue_loads_b(c + 2);
