@@ -94,6 +94,11 @@ SMALL = [
     ("bf16", 130, 64, 64, 4, 16, True, True),
     ("bf16", 150, 64, 128, 1, 32, True, True),
     ("bf16", 100, 32, 16, 2, 32, True, False),
+    # the tensor-core path without theta and / or lambda (no rotation: the checkpoint
+    # run loads B and x in one part)
+    ("bf16", 150, 64, 64, 1, 64, False, False),
+    ("bf16", 130, 64, 64, 2, 32, True, False),
+    ("bf16", 77, 64, 64, 4, 16, False, True),
     # state sizes that leave a partial 4-wide register tile (N % 4 == 2), narrow heads
     ("f32", 77, 12, 6, 1, 16, True, True),
     ("f32", 50, 4, 2, 2, 16, True, True),
