@@ -311,8 +311,8 @@ bool make_map_theta_plain(CUtensorMap* m, const void* base, const m3_dims& d, in
 int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float* A, const void* B, const void* C,
                   const float* lam, const void* theta, const void* dy, const float* dfinal, void* dx, float* ddt,
                   float* dA, void* dB, void* dC, float* dlam, void* dtheta, const m3bwd::Work& w, cudaStream_t s) {
-    // pass 1: the forward tensor-core kernel with chunk checkpoints (its y goes
-    // to dx, which pass 2 overwrites)
+    // pass 1: the forward tensor-core kernel's checkpoint run (the chunk states and
+    // angles only; dx is passed as its y but not written)
     int rc = m3ws::launch(*d, x, dt, A, B, C, lam, theta, nullptr, nullptr, nullptr, dx, nullptr, s, nullptr,
                           nullptr, nullptr, nullptr, 0.0f, w.G, w.phi);
     if (rc != M3_OK) return rc;

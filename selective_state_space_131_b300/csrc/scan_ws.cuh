@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
     using CF = Cfg<NSLAB, R, ROT, NORM>;
     // CKPT: the backward pass's checkpoint run, which needs the chunk states and
     // angles only: C is not loaded, and S, the mask, Y_intra, Y_inter and the
-    // output are skipped
+    // output are skipped; map_y then describes the fp32 checkpoints
+    // [b h (nch + 1)][N][P] (box 32 x 64 x 1, 128-byte swizzle), which leave
+    // through a shared-memory tile by TMA stores
     static_assert(!(CKPT && NORM), "no checkpoint run with the fused normalisation");
     constexpr int Q = CF::Q, N = CF::N, K = CF::K, TILE = CF::TILE;
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -898,11 +900,15 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             }   // !CKPT
             // (3) G_c = exp(cs_end) G_{c-1} + dG_c (fp32)
             if constexpr (CKPT) {
-                // G_{c-1} for the backward pass (rows and columns as held here)
-                float* dst = prm.ck_G + (((int64_t)unit * (nch + 1) + c) * N + g_row) * kP + ((N == 64) ? hc * 32 : 0);
+                // G_{-1} for the backward pass (rows and columns as held here); the later
+                // checkpoints leave through the staging tile below
+                if (c == 0) {
+                    float* dst = prm.ck_G + (((int64_t)unit * (nch + 1)) * N + g_row) * kP + ((N == 64) ? hc * 32 : 0);
 #pragma unroll
-                for (int p4 = 0; p4 < GC / 4; ++p4)
-                    *reinterpret_cast<float4*>(dst + 4 * p4) = make_float4(G[4 * p4], G[4 * p4 + 1], G[4 * p4 + 2], G[4 * p4 + 3]);
+                    for (int p4 = 0; p4 < GC / 4; ++p4)
+                        *reinterpret_cast<float4*>(dst + 4 * p4) =
+                            make_float4(G[4 * p4], G[4 * p4 + 1], G[4 * p4 + 2], G[4 * p4 + 3]);
+                }
             }
             __syncwarp();
             {
@@ -940,8 +946,29 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
             if (ptx::bar_sync_or(kBarWG1, kWG, fail || abort_s)) { aborted = true; break; }
             if (leader) ptx::mbar_arrive(&bar_dgfree);
             if constexpr (CKPT) {
+                static_assert(!CKPT || N == 64, "checkpoint run: N = 64");
                 // no output: the S/Y buffer of stage s (it held Phi_c only) is free
                 if (leader) ptx::mbar_arrive(&bar_syfree[s]);
+                if (c + 1 < nch) {
+                    // G_c (checkpoint slot c + 1) into the staging tile (the S', G and y
+                    // buffers, unused here): two [64 rows][32 floats] boxes, 128-byte
+                    // swizzled (conflict-free: the eight rows of a quarter-warp land in
+                    // eight 16-byte columns); the previous stores have read it (the
+                    // leader waited before the barrier above)
+                    uint8_t* box = smem + CF::OFF_SP + hc * (64 * 128);
+#pragma unroll
+                    for (int p4 = 0; p4 < 8; ++p4)
+                        *reinterpret_cast<float4*>(box + g_row * 128 + ((p4 ^ (g_row & 7)) << 4)) =
+                            make_float4(G[4 * p4], G[4 * p4 + 1], G[4 * p4 + 2], G[4 * p4 + 3]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::bar_sync(kBarWG1, kWG);
+                    if (leader) {
+                        const int slot = (int)((int64_t)unit * (nch + 1) + c + 1);
+                        ptx::tma_store_3d(&map_y, smem + CF::OFF_SP, 0, 0, slot);
+                        ptx::tma_store_3d(&map_y, smem + CF::OFF_SP + 64 * 128, 32, 0, slot);
+                        ptx::bulk_commit();
+                    }
+                }
                 continue;
             }
             if (tid == kYIssuer) {
@@ -1219,8 +1246,20 @@ inline int launch(const m3_dims& d, const void* x, const float* dt, const float*
     prm.ck_phi = ck_phi;
     const bool norm = norm_wB != nullptr;
     if (ck_G) {
-        // the checkpointing forward of the backward pass: N = 64, no normalisation
+        // the checkpointing forward of the backward pass: N = 64, no normalisation;
+        // no y, the map of the fp32 checkpoints [b h (nch + 1)][N][P] instead
         if (d.dstate != 64 || norm) return M3_ERR_UNSUPPORTED;
+        if (reinterpret_cast<uintptr_t>(ck_G) & 15u) return M3_ERR_ALIGN;
+        const int64_t slots = d.batch * d.heads * (int64_t)(prm.nchunks + 1);
+        if (slots >= INT32_MAX) return M3_ERR_UNSUPPORTED;
+        cuuint64_t dims[3] = {(cuuint64_t)kP, 64, (cuuint64_t)slots};
+        cuuint64_t strides[2] = {(cuuint64_t)kP * 4, (cuuint64_t)64 * kP * 4};
+        cuuint32_t box[3] = {32, 64, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (encode_fn()(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ck_G, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return M3_ERR_CUDA;
         return rot ? launch_r<1, true, false, true>(d, maps, prm, s) : launch_r<1, false, false, true>(d, maps, prm, s);
     }
     if (d.dstate == 64)
