@@ -318,10 +318,13 @@ int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float*
     if (rc != M3_OK) return rc;
     // pass 2
     const int Q = m3ws::kRows / (int)d->rank;
-    CUtensorMap maps[5];
+    CUtensorMap maps[8];
     memset(maps, 0, sizeof(maps));
+    // inputs: x, B, C, dy, theta; the gradient tiles the kernel stores: dx, dB, dC
     if (!m3ws::make_map5(&maps[0], x, *d, 64, Q) || !m3ws::make_map5(&maps[1], B, *d, 64, Q) ||
-        !m3ws::make_map5(&maps[2], C, *d, 64, Q) || !m3ws::make_map5(&maps[3], dy, *d, 64, Q))
+        !m3ws::make_map5(&maps[2], C, *d, 64, Q) || !m3ws::make_map5(&maps[3], dy, *d, 64, Q) ||
+        !m3ws::make_map5(&maps[5], dx, *d, 64, Q) || !m3ws::make_map5(&maps[6], dB, *d, 64, Q) ||
+        !m3ws::make_map5(&maps[7], dC, *d, 64, Q))
         return M3_ERR_CUDA;
     if (theta) {
         if (!make_map_theta_plain(&maps[4], theta, *d, Q)) return M3_ERR_CUDA;
@@ -353,7 +356,8 @@ int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float*
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, m3bwdtc::SMEM_BYTES) !=       \
             cudaSuccess)                                                                                       \
             return M3_ERR_CUDA;                                                                                \
-        k<<<grid, m3bwdtc::kThreads, m3bwdtc::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], prm); \
+        k<<<grid, m3bwdtc::kThreads, m3bwdtc::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],     \
+                                                               maps[5], maps[6], maps[7], prm);                \
     }
     switch (d->rank) {
         case 1: M3_BWD_TC(1); break;

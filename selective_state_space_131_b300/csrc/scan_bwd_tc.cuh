@@ -152,7 +152,9 @@ template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     m3_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_B,
                      const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_dy,
-                     const __grid_constant__ CUtensorMap map_th, const Params prm) {
+                     const __grid_constant__ CUtensorMap map_th, const __grid_constant__ CUtensorMap map_dx,
+                     const __grid_constant__ CUtensorMap map_dB, const __grid_constant__ CUtensorMap map_dC,
+                     const Params prm) {
     constexpr int Q = kT / R;      // tokens per chunk
     constexpr int K = 32;          // rotation pairs (N = 64)
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -446,10 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // ---- (2) the tiles are in; rotate B, C in place (B~, C~) and write B~' and C~'
+        //      (the previous chunk's gradient stores have read the C~', S' and dS tiles)
         if (!ptx::mbar_wait(&bar_ld[st], ((nch - 1 - c) >> 1) & 1, kWaitBudget)) {
             m3::set_status(m3::kStatusWaitTimeout);
             abort_s = 1;
         }
+        if (tid == 0) ptx::bulk_wait_read0();
         __syncthreads();
         if (abort_s) { fail = true; break; }
         {
@@ -795,17 +799,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld16x2_32(tmem + lane_base + TM_DX, vx);
             ptx::tmem_ld16x2_32(tmem + lane_base + TM_DGU, vg);
             ptx::tmem_ld_wait();
-            const int tj = row / R;
-            if (tj < nt) {
-                __nv_bfloat16* dst = prm.dx + (tok_idx(t0 + tj) * R + (row - tj * R)) * 64 + 32 * hc;
+            // dx of row j into the staging tile (the S' buffer, free once the masked
+            // products are done; rows past the sequence end are clipped by the store)
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    reinterpret_cast<uint4*>(dst)[g] =
-                        make_uint4(pack2(__uint_as_float(vx[8 * g]), __uint_as_float(vx[8 * g + 1])),
-                                   pack2(__uint_as_float(vx[8 * g + 2]), __uint_as_float(vx[8 * g + 3])),
-                                   pack2(__uint_as_float(vx[8 * g + 4]), __uint_as_float(vx[8 * g + 5])),
-                                   pack2(__uint_as_float(vx[8 * g + 6]), __uint_as_float(vx[8 * g + 7])));
-            }
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4*>(smem + OFF_SP + swz(row, 4 * hc + g)) =
+                    make_uint4(pack2(__uint_as_float(vx[8 * g]), __uint_as_float(vx[8 * g + 1])),
+                               pack2(__uint_as_float(vx[8 * g + 2]), __uint_as_float(vx[8 * g + 3])),
+                               pack2(__uint_as_float(vx[8 * g + 4]), __uint_as_float(vx[8 * g + 5])),
+                               pack2(__uint_as_float(vx[8 * g + 6]), __uint_as_float(vx[8 * g + 7])));
             const float dec = m3::ex2_approx(F[F_CS + Q - 1]);
 #pragma unroll
             for (int p = 0; p < 32; ++p) dG[p] = fmaf(dec, dG[p], __uint_as_float(vg[p]));
@@ -832,7 +834,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d_oi[r] = F[F_DSD + (t * R + r) * 4 + (row - t * R)];
             }
             const bool fin = (c == nch - 1) && t == nt - 1;
-            const int64_t gi = (tok_idx(t0 + t) * R + (row - t * R)) * 64 + 32 * hc;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float cr[8], br[8], cdg[8], bdg[8];
@@ -870,18 +871,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // d/dphi Rot(-phi) v = (v~_1, -v~_0)
                     F[F_DPR + row * KS + k] = fb0 * br[e + 1] - fb1 * br[e] + fc0 * cr[e + 1] - fc1 * cr[e];
                 }
-                if (t < nt) {
-                    reinterpret_cast<uint4*>(prm.dC + gi)[g] = make_uint4(pc[0], pc[1], pc[2], pc[3]);
-                    reinterpret_cast<uint4*>(prm.dB + gi)[g] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-                }
+                // into the staging tiles (the dS and C~' buffers, free here)
+                *reinterpret_cast<uint4*>(smem + OFF_DS + swz(row, 4 * hc + g)) = make_uint4(pc[0], pc[1], pc[2], pc[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_CD + swz(row, 4 * hc + g)) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
             }
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
+        if (tid == 0) {
+            // dx, dC, dB of the chunk: one TMA store each from the staging tiles
+            // (their reads are waited for before the tiles are written again)
+            ptx::tma_store_5d(&map_dx, smem + OFF_SP, 0, 0, h, (int)t0, b);
+            ptx::tma_store_5d(&map_dC, smem + OFF_DS, 0, 0, h, (int)t0, b);
+            ptx::tma_store_5d(&map_dB, smem + OFF_CD, 0, 0, h, (int)t0, b);
+            ptx::bulk_commit();
+        }
         __syncthreads();
     }
+    if (tid == 0) ptx::bulk_wait0();   // every gradient tile stored
     // dtheta of chunk 0 (the last chunk processed)
     if (!fail && wg == 0 && prm.theta) dtheta_chunk(0);
     if (tid == 128) prm.dA_part[unit] = dA_acc;   // warp 4 lane 0 accumulated it
