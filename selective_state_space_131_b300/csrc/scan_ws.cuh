@@ -101,11 +101,14 @@ struct Cfg {
     static constexpr int OFF_G = OFF_SP + TILE;               // G bf16 [N][P] (MN-major)
     static constexpr int OFF_Y = OFF_G + N * 128;             // y staging (TMA store source)
     static constexpr int OFF_L = OFF_Y + TILE;                // L: [64 rows][64 tokens] 0/1, K-major
-    static constexpr int OFF_SC = OFF_L + TILE;               // per-stage scalars
+    // per-chunk scalars in three buffers (chunk c in buffer c % 3): warp 0 writes chunk
+    // c's while warpgroup 1 may still read chunk c - 1's and c - 2's (a warpgroup-0
+    // warp that starts chunk c knows only that chunk c - 3's output has been stored)
+    static constexpr int OFF_SC = OFF_L + TILE;
     static constexpr int SC_CS = 0, SC_W = Q, SC_GAM = 2 * Q, SC_SCB = 3 * Q, SC_SCF = 4 * Q, SC_SDF = 5 * Q,
                          SC_DEC = 6 * Q;
-    static constexpr int SC_STRIDE = 6 * Q + 4;               // floats per stage
-    static constexpr int OFF_CARRY = align16(OFF_SC + 2 * SC_STRIDE * 4);  // float [2][K]: angle carry
+    static constexpr int SC_STRIDE = 6 * Q + 4;               // floats per buffer
+    static constexpr int OFF_CARRY = align16(OFF_SC + 3 * SC_STRIDE * 4);  // float [2][K]: angle carry
     // dt and lambda of a chunk's Q tokens and the token after it, per stage: float [2][2][DL]
     static constexpr int DL = (Q + 1 + 3) & ~3;
     static constexpr int OFF_DL = OFF_CARRY + 2 * K * 4;
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             uint8_t* st = smem + s * CF::ST_BYTES;
-            float* sc = scal0 + s * CF::SC_STRIDE;
+            float* sc = scal0 + (c % 3) * CF::SC_STRIDE;
             const uint32_t tm_sy = tmem + CF::TM_SY0 + 64u * s;
             // (0) thread kEarlyIssuer, once chunk c-2's output has been read (its S/Y buffer and
             //     Y_inter free): Phi_rows = L theta -> TMEM S/Y[s] when chunk c's tiles
@@ -812,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1;
             uint8_t* st = smem + s * CF::ST_BYTES;
-            const float* sc = scal0 + s * CF::SC_STRIDE;
+            const float* sc = scal0 + (c % 3) * CF::SC_STRIDE;
             const uint32_t tm_sy = tmem + lane_base + CF::TM_SY0 + 64u * s;
             // (1) S_c and dG_c are in TMEM
             bool fail = !ptx::mbar_wait(&bar_sd[s], (c >> 1) & 1, kWaitBudget);
