@@ -140,6 +140,38 @@ def test_bwd_deterministic(m3):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("R", [1, 4])
+def test_bwd_repeated_runs_write_every_gradient_the_same(m3, R):
+    """30 backward passes of the tensor-core path into gradient buffers pre-filled
+    with NaN (and a NaN-filled workspace): every element written and every run
+    bit-identical to the first -- a check on the checkpoint and gradient tiles
+    that leave through shared memory by TMA stores."""
+    shape = inputs.ScanShape(batch=2, seqlen=150, heads=3, headdim=64, dstate=64, rank=R, chunk=64 // R, dtype="bf16")
+    inp = inputs.make_scan_inputs(shape, 895 + R)
+    dy, dfinal = upstream(shape, 896 + R)
+    d = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    dims = m3.scan_dims(d["x"], d["B"], 64 // R)
+    wsb = m3.m3_scan_bwd_workspace_size(dims)
+    dyc, dfc = dy.cuda(), dfinal.cuda()
+    ref = None
+    for it in range(30):
+        ws = torch.full((wsb // 4,), float("nan"), device="cuda")
+        out = {"dx": d["x"], "ddt": d["dt"], "dA": d["A"], "dB": d["B"], "dC": d["C"], "dlam": d["lam"],
+               "dtheta": d["theta"]}
+        out = {k: torch.full_like(v, float("nan")) for k, v in out.items()}
+        m3.m3_scan_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["lam"], d["theta"], dyc, dfc, out["dx"],
+                       out["ddt"], out["dA"], out["dB"], out["dC"], out["dlam"], out["dtheta"], ws, wsb, dims=dims)
+        if ref is None:
+            torch.cuda.synchronize()
+            for k, v in out.items():
+                assert not torch.isnan(v.float()).any(), k
+            ref = out
+        else:
+            for k in out:
+                assert torch.equal(out[k], ref[k]), (it, k)
+    assert m3.m3_device_status() == m3.M3_OK
+
+
 def test_bwd_siso_workload_full_size(m3):
     """The SISO complex + trapezoidal workload (b8 h32 T8192 P64 N64, bf16) at
     full size -- the launch the bench times -- checked on three heads for every
