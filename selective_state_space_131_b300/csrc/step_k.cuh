@@ -246,7 +246,6 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                 cf[0] = c0.x; cf[1] = c0.y; cf[2] = c0.z; cf[3] = c0.w;
                 cf[4] = c1.x; cf[5] = c1.y; cf[6] = c1.z; cf[7] = c1.w;
             }
-            const bool upd = j + 1 < a.k;   // the last token leaves h', not g
             float xr[R][4];
 #pragma unroll
             for (int r = 0; r < R; ++r) SVec<T>::ld4(cur + (r * P + p0) * es, xr[r]);
@@ -284,8 +283,10 @@ __global__ void __launch_bounds__(MAXT, min_ctas(R, MAXT)) m3_step_k_kernel(Step
                     for (int r = 0; r < R; ++r)
                         yp[r][hv] = __ffma2_rn(make_float2(cr[r].x, cr[r].x), o0,
                                                __ffma2_rn(make_float2(cr[r].y, cr[r].y), o1, yp[r][hv]));
-                    h0[hv] = upd ? __ffma2_rn(c2, u0, o0) : o0;
-                    h1[hv] = upd ? __ffma2_rn(c2, u1, o1) : o1;
+                    // g = h' + c_next u; c_next is 0 after the launch's last token, which
+                    // so leaves h' (up to the sign of an exact zero)
+                    h0[hv] = __ffma2_rn(c2, u0, o0);
+                    h1[hv] = __ffma2_rn(c2, u1, o1);
                 }
             }
             // y of token j: lanes P4 apart, then the warps through shared memory
