@@ -16,9 +16,12 @@
 // Every operand is one 64 x 64 bf16 tile, 128-byte swizzled, stored [row][col]
 // and read K-major or MN-major as the product needs (as in scan_ws.cuh).
 // 256 threads: the two warpgroups read different accumulators in the
-// epilogues; thread 0 issues the MMAs, thread 32 the TMA loads.  Waits are
-// bounded: a wait that runs out sets the device status word, the stop is voted
-// at the next barrier, and the CTA waits (bounded) for its work in flight.
+// epilogues; thread 32 issues the MMAs and the TMA loads, thread 0 the bulk
+// copies of the checkpoints and the TMA stores of each chunk's dx, dB and dC
+// tiles (staged in the S', dS and C~' buffers once the products that read them
+// are done).  Waits are bounded: a wait that runs out sets the device status
+// word, the stop is voted at the next barrier, and the CTA waits (bounded) for
+// its work in flight.
 #pragma once
 
 #include <cuda.h>

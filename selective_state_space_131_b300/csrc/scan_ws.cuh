@@ -393,15 +393,15 @@ __global__ void __launch_bounds__(kThreads, (NSLAB == 1 ? 2 : 1))
 
     if (tid < kWG) {
         // ======================= warpgroup 0: prologue + S / dG issue =======================
-        // Thread 0 turns the chunk's theta tile into the cumulative angles of
-        // every tile row with one MMA, Phi_rows = L theta (L[i][t] = 1 for
+        // Lane 0 of warp 1 turns the chunk's theta tile into the cumulative angles
+        // of every tile row with one MMA, Phi_rows = L theta (L[i][t] = 1 for
         // t <= token(i)), into the S/Y TMEM buffer of the stage.  Thread
         // (warp w, lane l) then owns tile row 16 w + l % 16 and the rotation
         // pairs [PH (l / 16), PH (l / 16) + PH): it reads those angles with the
         // 16x32bx2 TMEM shape, rotates its half of the B and C rows in shared
         // memory (bank-conflict free under the 128-byte swizzle) and writes its
-        // half of the scaled copy B~'.  Every warp computes the chunk scalars
-        // itself (lane l holds tokens l and l + 32).
+        // half of the scaled copy B~'.  Warp 0 computes the chunk scalars (lane l
+        // holds tokens l and l + 32) into the chunk's scalar buffer.
         constexpr int PH = K / 2;               // pairs per thread
         constexpr int GPT = PH / 4;             // 16-byte groups per thread
         const int row = warp * 16 + (lane & 15);
