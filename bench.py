@@ -41,9 +41,9 @@ HBM_FALLBACK_GBS = 6400.0
 # source is unchanged, else null.  Captured at T = 2048 and scaled x4 to
 # T = 8192 (traffic grows with the sequence length).
 NCU_TRAFFIC = {
-    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.215360e6 + 48.333568e6),
+    "m3_siso_bf16_b8h32T8192P64N64": {"bytes": 4 * (239.238144e6 + 48.558336e6),
                                       "source": "selective_state_space_131_b300/csrc/scan_ws.cuh",
-                                      "sha256": "732d467261355bc1"},
+                                      "sha256": "5570e514627f945e"},
     # decode: one step of the 1024-step sweep (graph replay), per launch
     "decode_f32_b256h32P64N64_R1": {"bytes": 145.839360e6 + 76.878080e6,
                                     "source": "selective_state_space_131_b300/csrc/step_fast.cuh",
