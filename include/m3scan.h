@@ -239,8 +239,11 @@ M3_API size_t m3_scan_bwd_workspace_size(const m3_dims* d);
  * the chunk states into the workspace; a second pass walks the chunks in
  * reverse and differentiates the chunked form (the intra-chunk mask, the
  * inter-chunk term, the state update, the trapezoid weights, the cumulative
- * rotation); a third sums dA over the batch.  fp32 arithmetic on CUDA cores,
- * deterministic (fixed-order sums).
+ * rotation); a third sums dA over the batch.  bf16 with N = P = 64, R in
+ * {1, 2, 4}, chunk R = 64 and x, B, C, theta, dy, dx, dB, dC, dtheta 16-byte
+ * aligned runs the chunk products on the tensor cores (bf16 operands, fp32
+ * accumulators and epilogues); every other case in fp32 on CUDA cores.  Both
+ * are deterministic (fixed-order sums).
  *   x, dt, A, B, C, lambda, theta   the forward's inputs (as in m3_scan_fwd)
  *   dy      [b, T, h, R, P]  dtype        dfinal [b, h, N, P] fp32 or NULL (0)
  *   dx      [b, T, h, R, P]  dtype        ddt    [b, T, h]    fp32

@@ -318,18 +318,20 @@ int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float*
     if (rc != M3_OK) return rc;
     // pass 2
     const int Q = m3ws::kRows / (int)d->rank;
-    CUtensorMap maps[8];
+    CUtensorMap maps[9];
     memset(maps, 0, sizeof(maps));
-    // inputs: x, B, C, dy, theta; the gradient tiles the kernel stores: dx, dB, dC
+    // inputs: x, B, C, dy, theta; the gradient tiles the kernel stores: dx, dB, dC, dtheta
     if (!m3ws::make_map5(&maps[0], x, *d, 64, Q) || !m3ws::make_map5(&maps[1], B, *d, 64, Q) ||
         !m3ws::make_map5(&maps[2], C, *d, 64, Q) || !m3ws::make_map5(&maps[3], dy, *d, 64, Q) ||
         !m3ws::make_map5(&maps[5], dx, *d, 64, Q) || !m3ws::make_map5(&maps[6], dB, *d, 64, Q) ||
         !m3ws::make_map5(&maps[7], dC, *d, 64, Q))
         return M3_ERR_CUDA;
     if (theta) {
-        if (!make_map_theta_plain(&maps[4], theta, *d, Q)) return M3_ERR_CUDA;
+        if (!make_map_theta_plain(&maps[4], theta, *d, Q) || !make_map_theta_plain(&maps[8], dtheta, *d, Q))
+            return M3_ERR_CUDA;
     } else {
         maps[4] = maps[0];   // never read
+        maps[8] = maps[0];   // never written
     }
     m3bwdtc::Params prm;
     prm.T = d->seqlen;
@@ -357,7 +359,7 @@ int launch_bwd_tc(const m3_dims* d, const void* x, const float* dt, const float*
             cudaSuccess)                                                                                       \
             return M3_ERR_CUDA;                                                                                \
         k<<<grid, m3bwdtc::kThreads, m3bwdtc::SMEM_BYTES, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4],     \
-                                                               maps[5], maps[6], maps[7], prm);                \
+                                                               maps[5], maps[6], maps[7], maps[8], prm);       \
     }
     switch (d->rank) {
         case 1: M3_BWD_TC(1); break;
@@ -378,8 +380,8 @@ int launch_bwd(const m3_dims* d, const void* x, const float* dt, const float* A,
     const int64_t units = d->batch * d->heads;
     const m3bwd::Work w = m3bwd::work_split(ws, units, g);
     if constexpr (sizeof(T) == 2) {
-        const void* tma_ptrs[] = {x, B, C, theta, dy, dx, dB, dC};
-        if (bwd_tc_shape(d, tma_ptrs, 8))
+        const void* tma_ptrs[] = {x, B, C, theta, dy, dx, dB, dC, dtheta};
+        if (bwd_tc_shape(d, tma_ptrs, 9))
             return launch_bwd_tc(d, x, dt, A, B, C, lam, theta, dy, dfinal, dx, ddt, dA, dB, dC, dlam, dtheta, w, s);
     }
     auto k1 = m3bwd::m3_bwd_ckpt_kernel<T>;

@@ -74,7 +74,8 @@ constexpr int F_SEG = F_CZE + 64;                                               
 constexpr int F_DSD = F_SEG + 128;                                                       // [64][4] dS, same-token block
 constexpr int F_END = F_DSD + 256;
 constexpr int OFF_GB = (OFF_F + F_END * 4 + 1023) & ~1023;   // fp32 G checkpoint, 2 stages x [64][64]
-constexpr int SMEM_BYTES = OFF_GB + 2 * 64 * 64 * 4 + 1024;
+constexpr int OFF_DTH = OFF_GB + 2 * 64 * 64 * 4;   // bf16 [64 tokens][32 pairs]: dtheta staging
+constexpr int SMEM_BYTES = OFF_DTH + 64 * 32 * 2 + 1024;
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_DSP = 64, TM_T2 = 128, TM_XG = 192, TM_DX = 256, TM_DC = 320, TM_DB = 384,
                    TM_DGU = 448, TM_COLS = 512;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap map_C, const __grid_constant__ CUtensorMap map_dy,
                      const __grid_constant__ CUtensorMap map_th, const __grid_constant__ CUtensorMap map_dx,
                      const __grid_constant__ CUtensorMap map_dB, const __grid_constant__ CUtensorMap map_dC,
-                     const Params prm) {
+                     const __grid_constant__ CUtensorMap map_dth, const Params prm) {
     constexpr int Q = kT / R;      // tokens per chunk
     constexpr int K = 32;          // rotation pairs (N = 64)
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -234,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int seg = warp;
         constexpr int RS = 16;
         const int64_t tc0 = (int64_t)cc * Q;
-        const int ntc = (int)((T - tc0) < Q ? (T - tc0) : Q);
+        __nv_bfloat16* dth = reinterpret_cast<__nv_bfloat16*>(smem + OFF_DTH);   // [token][pair]
+        // the previous chunk's dtheta store has read the staging tile before the
+        // barrier below lets any thread write it
+        if (tid == 0) ptx::bulk_wait_read0();
         float v[RS];
         float tot = 0.0f;
 #pragma unroll
@@ -250,11 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = RS - 1; q >= 0; --q) {
             const int rw = seg * RS + q;
             acc += v[q];
-            if (rw % R == 0 && rw / R < ntc)
-                prm.dtheta[(((int64_t)b * T + tc0 + rw / R) * prm.H + h) * K + lane] = __float2bfloat16_rn(acc);
+            if (rw % R == 0) dth[(rw / R) * K + lane] = __float2bfloat16_rn(acc);   // past T: clipped
         }
-        ptx::bar_sync(3, 128);   // every thread has read F_DPHI
+        ptx::fence_proxy_async_smem();
+        ptx::bar_sync(3, 128);   // every thread has read F_DPHI and written its dtheta
         if (seg == 0) F[F_DPHI + lane] = acc;
+        if (tid == 0) {
+            // the chunk's dtheta [Q tokens][32 pairs] in one TMA store
+            ptx::tma_store_4d(&map_dth, dth, 0, h, (int)tc0, b);
+            ptx::bulk_commit();
+        }
     };
     auto issue_scalars = [&](int c, int st) {
         float* dst = F + F_DL + st * 2 * 68;
@@ -893,9 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
     }
-    if (tid == 0) ptx::bulk_wait0();   // every gradient tile stored
     // dtheta of chunk 0 (the last chunk processed)
     if (!fail && wg == 0 && prm.theta) dtheta_chunk(0);
+    if (tid == 0) ptx::bulk_wait0();   // every gradient tile stored
     if (tid == 128) prm.dA_part[unit] = dA_acc;   // warp 4 lane 0 accumulated it
     if (fail && tid == 0) {
         // stopped early: the checkpoint copies in flight land (bounded wait)
