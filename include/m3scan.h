@@ -85,7 +85,7 @@ typedef struct {
 #define M3_ERR_DTYPE (-3)       /* unknown dtype */
 #define M3_ERR_ALIGN (-4)       /* a pointer is not aligned as required */
 #define M3_ERR_CUDA (-5)        /* a CUDA call or launch failed (no device, ...) */
-#define M3_ERR_UNSUPPORTED (-6) /* valid sizes this build has no kernel for */
+#define M3_ERR_UNSUPPORTED (-6) /* valid sizes no kernel of the library takes */
 #define M3_ERR_DEVICE (-7)      /* the device status word was set */
 #define M3_ERR_WORKSPACE (-8)   /* workspace too small */
 #define M3_ERR_VALUE (-9)       /* a scalar argument is out of range (e.g. a negative epsilon) */
@@ -98,7 +98,7 @@ typedef struct {
 #define M3_ALGO_CHUNKED_SIMT 2    /* chunked kernel on CUDA cores, fp32 arithmetic */
 
 /* Bytes of device workspace m3_scan_fwd needs for `d` (0 for every forward
- * kernel of this build).  Returns 0 for invalid dims as well. */
+ * kernel of the library).  Returns 0 for invalid dims as well. */
 M3_API size_t m3_scan_workspace_size(const m3_dims* d);
 
 /* Which prefill kernel m3_scan_fwd runs for `d` (M3_ALGO_NONE for invalid
