@@ -485,20 +485,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t ob[4], oc[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    float b0 = lo16(pb[m]), b1 = hi16(pb[m]), c0 = lo16(pc[m]), c1 = hi16(pc[m]);
+                    // the B and C pairs side by side in packed fp32: u = (a_B, a_C), v = (b_B, b_C)
+                    float2 u = make_float2(lo16(pb[m]), lo16(pc[m])), v = make_float2(hi16(pb[m]), hi16(pc[m]));
                     if (prm.theta) {
                         const int k = g * 4 + m;
                         const float co = F[F_COS + t * KS + k], si = F[F_SIN + t * KS + k];
                         // Rot(-phi): (a, b) -> (a cos + b sin, -a sin + b cos)
-                        const float nb0 = fmaf(b0, co, b1 * si), nb1 = fmaf(-b0, si, b1 * co);
-                        const float nc0 = fmaf(c0, co, c1 * si), nc1 = fmaf(-c0, si, c1 * co);
-                        b0 = nb0; b1 = nb1; c0 = nc0; c1 = nc1;
+                        const float2 co2 = make_float2(co, co), si2 = make_float2(si, si), nsi2 = make_float2(-si, -si);
+                        const float2 nu = __ffma2_rn(u, co2, __fmul2_rn(v, si2));
+                        const float2 nv = __ffma2_rn(u, nsi2, __fmul2_rn(v, co2));
+                        u = nu;
+                        v = nv;
                     }
-                    pb[m] = pack2(b0, b1);
-                    pc[m] = pack2(c0, c1);
+                    pb[m] = pack2(u.x, v.x);
+                    pc[m] = pack2(u.y, v.y);
                     // scaled copies from the rounded values the MMAs see
-                    ob[m] = pack2(lo16(pb[m]) * sj, hi16(pb[m]) * sj);
-                    oc[m] = pack2(lo16(pc[m]) * ei, hi16(pc[m]) * ei);
+                    const float2 sb = __fmul2_rn(make_float2(lo16(pb[m]), hi16(pb[m])), make_float2(sj, sj));
+                    const float2 scl = __fmul2_rn(make_float2(lo16(pc[m]), hi16(pc[m])), make_float2(ei, ei));
+                    ob[m] = pack2(sb.x, sb.y);
+                    oc[m] = pack2(scl.x, scl.y);
                 }
                 *reinterpret_cast<uint4*>(tb + off) = vb;
                 *reinterpret_cast<uint4*>(tc + off) = vc;
