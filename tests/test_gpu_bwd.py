@@ -94,6 +94,11 @@ SMALL = [
     ("bf16", 130, 64, 64, 4, 16, True, True),
     ("bf16", 150, 64, 128, 1, 32, True, True),
     ("bf16", 100, 32, 16, 2, 32, True, False),
+    # the tensor-core path on sequences of one partial chunk, exactly one chunk and
+    # one chunk plus a token (the gradient tiles' TMA stores clip the rows past T)
+    ("bf16", 5, 64, 64, 1, 64, True, True),
+    ("bf16", 32, 64, 64, 2, 32, True, True),
+    ("bf16", 17, 64, 64, 4, 16, True, True),
     # the tensor-core path without theta and / or lambda (no rotation: the checkpoint
     # run loads B and x in one part)
     ("bf16", 150, 64, 64, 1, 64, False, False),
